@@ -1,0 +1,237 @@
+"""Exact fused scaled-dot-product attention (bf16) for NVIDIA GB300 (sm_103a).
+
+The compute lives in libattn_gb300.so (hand-written CUDA: TMA, tcgen05 MMAs
+with Tensor Memory accumulators, warp-specialised pipelines); see
+include/attn.h for the C ABI. This package is a thin binding with the same
+entry-point names: it only marshals torch tensors (device memory, strides,
+the current CUDA stream) into the C parameter structs. Nothing here computes
+attention, and there is no CPU or library fallback: if the shared library is
+missing, importing this package raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Tuple
+
+import torch
+
+from . import _abi
+from ._abi import AttnBwdParams, AttnError, AttnFwdParams  # noqa: F401
+
+_lib = _abi.load()
+
+SUPPORTED_HEAD_DIMS = ((64, 64), (128, 128), (192, 128))
+
+__all__ = [
+    "attn_fwd", "attn_fwd_varlen", "attn_bwd", "attn_bwd_varlen", "attn_exp2_eval",
+    "attn_get_device_status", "attention", "AttnError", "SUPPORTED_HEAD_DIMS", "library_path",
+]
+
+
+def library_path() -> str:
+    return _abi.LIB_PATH
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _check_bf16(name: str, t: torch.Tensor, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if t.stride(-1) != 1:
+        raise ValueError(f"{name}: head_dim must be contiguous")
+
+
+def _strides4(t: torch.Tensor):
+    # [B, N, H, d] -> (batch, row, head) element strides
+    return t.stride(0), t.stride(1), t.stride(2)
+
+
+def _strides3(t: torch.Tensor):
+    # packed [total, H, d] -> batch stride unused
+    return 0, t.stride(0), t.stride(1)
+
+
+def _fill_fwd(p: AttnFwdParams, q, k, v, o, lse, strides, scale, causal):
+    p.q, p.k, p.v, p.o, p.lse = _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse)
+    (p.q_batch_stride, p.q_row_stride, p.q_head_stride) = strides(q)
+    (p.k_batch_stride, p.k_row_stride, p.k_head_stride) = strides(k)
+    (p.v_batch_stride, p.v_row_stride, p.v_head_stride) = strides(v)
+    (p.o_batch_stride, p.o_row_stride, p.o_head_stride) = strides(o)
+    p.d_qk, p.d_v = q.shape[-1], v.shape[-1]
+    p.heads = q.shape[-2]
+    p.softmax_scale = scale
+    p.causal = 1 if causal else 0
+
+
+def _workspace(size: int, device) -> Tuple[Optional[torch.Tensor], int]:
+    if size == 0:
+        return None, 0
+    return torch.empty(size, dtype=torch.uint8, device=device), size
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = False,
+             softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+             lse: Optional[torch.Tensor] = None, rescale_stats: Optional[torch.Tensor] = None,
+             stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Dense forward. q [B, Nq, H, d_qk], k [B, Nk, H, d_qk], v [B, Nk, H, d_v] (bf16, CUDA).
+    Returns (O [B, Nq, H, d_v] bf16, LSE [B, H, Nq] fp32, natural log)."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_bf16(n, t, 4)
+    B, Nq, H, dqk = q.shape
+    Nk, dv = k.shape[1], v.shape[-1]
+    if k.shape != (B, Nk, H, dqk) or v.shape[:3] != (B, Nk, H):
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    scale = float(softmax_scale) if softmax_scale is not None else 1.0 / math.sqrt(dqk)
+    if out is None:
+        out = torch.empty((B, Nq, H, dv), dtype=torch.bfloat16, device=q.device)
+    _check_bf16("out", out, 4)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if lse.shape != (B, H, Nq) or not lse.is_contiguous() or lse.dtype != torch.float32:
+        raise ValueError("lse must be a contiguous float32 [B, H, Nq] tensor")
+    p = AttnFwdParams()
+    _fill_fwd(p, q, k, v, out, lse, _strides4, scale, causal)
+    p.batch, p.seqlen_q, p.seqlen_k = B, Nq, Nk
+    p.rescale_stats = _ptr(rescale_stats)
+    ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
+    _abi.check(_lib.attn_fwd(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                    cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, *, causal: bool = False,
+                    softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                    lse: Optional[torch.Tensor] = None, rescale_stats: Optional[torch.Tensor] = None,
+                    stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Packed variable-length forward. q [total_q, H, d_qk], k/v [total_k, H, d]; cu_seqlens int32 on
+    the device. Returns (O [total_q, H, d_v], LSE [H, total_q])."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_bf16(n, t, 3)
+    for n, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    tq, H, dqk = q.shape
+    tk, dv = k.shape[0], v.shape[-1]
+    scale = float(softmax_scale) if softmax_scale is not None else 1.0 / math.sqrt(dqk)
+    if out is None:
+        out = torch.empty((tq, H, dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((H, tq), dtype=torch.float32, device=q.device)
+    p = AttnFwdParams()
+    _fill_fwd(p, q, k, v, out, lse, _strides3, scale, causal)
+    p.cu_seqlens_q, p.cu_seqlens_k = _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)
+    p.num_seqs = cu_seqlens_q.numel() - 1
+    p.max_seqlen_q, p.max_seqlen_k = int(max_seqlen_q), int(max_seqlen_k)
+    p.total_q, p.total_k = tq, tk
+    p.batch = 1
+    p.rescale_stats = _ptr(rescale_stats)
+    ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
+    _abi.check(_lib.attn_fwd_varlen(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_fwd_varlen")
+    return out, lse
+
+
+def _fill_bwd(p: AttnBwdParams, do, dq, dk, dv, strides, deterministic):
+    p.dout, p.dq, p.dk, p.dv = _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv)
+    (p.do_batch_stride, p.do_row_stride, p.do_head_stride) = strides(do)
+    (p.dq_batch_stride, p.dq_row_stride, p.dq_head_stride) = strides(dq)
+    (p.dk_batch_stride, p.dk_row_stride, p.dk_head_stride) = strides(dk)
+    (p.dv_batch_stride, p.dv_row_stride, p.dv_head_stride) = strides(dv)
+    p.deterministic = 1 if deterministic else 0
+
+
+def attn_bwd(q, k, v, out, lse, dout, *, causal: bool = False, softmax_scale: Optional[float] = None,
+             deterministic: bool = False, dq=None, dk=None, dv=None, stream=None):
+    """Dense backward: returns (dQ, dK, dV) bf16 for the loss <O, dO>."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _check_bf16(n, t, 4)
+    B, Nq, H, dqk = q.shape
+    Nk = k.shape[1]
+    scale = float(softmax_scale) if softmax_scale is not None else 1.0 / math.sqrt(dqk)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    p = AttnBwdParams()
+    _fill_fwd(p.fwd, q, k, v, out, lse, _strides4, scale, causal)
+    p.fwd.batch, p.fwd.seqlen_q, p.fwd.seqlen_k = B, Nq, Nk
+    _fill_bwd(p, dout, dq, dk, dv, _strides4, deterministic)
+    ws, nbytes = _workspace(_lib.attn_bwd_workspace_size(ctypes.byref(p)), q.device)
+    _abi.check(_lib.attn_bwd(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int, *,
+                    causal: bool = False, softmax_scale: Optional[float] = None, deterministic: bool = False,
+                    dq=None, dk=None, dv=None, stream=None):
+    """Packed variable-length backward: returns (dQ, dK, dV) packed like q, k, v."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _check_bf16(n, t, 3)
+    tq, H, dqk = q.shape
+    scale = float(softmax_scale) if softmax_scale is not None else 1.0 / math.sqrt(dqk)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    p = AttnBwdParams()
+    _fill_fwd(p.fwd, q, k, v, out, lse, _strides3, scale, causal)
+    p.fwd.cu_seqlens_q, p.fwd.cu_seqlens_k = _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)
+    p.fwd.num_seqs = cu_seqlens_q.numel() - 1
+    p.fwd.max_seqlen_q, p.fwd.max_seqlen_k = int(max_seqlen_q), int(max_seqlen_k)
+    p.fwd.total_q, p.fwd.total_k = tq, k.shape[0]
+    p.fwd.batch = 1
+    _fill_bwd(p, dout, dq, dk, dv, _strides3, deterministic)
+    ws, nbytes = _workspace(_lib.attn_bwd_workspace_size(ctypes.byref(p)), q.device)
+    _abi.check(_lib.attn_bwd_varlen(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_bwd_varlen")
+    return dq, dk, dv
+
+
+def attn_exp2_eval(x: torch.Tensor, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Evaluates the kernels' software (Cody-Waite + cubic) and hardware exp2 on a float32 CUDA tensor."""
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    yp, yh = torch.empty_like(x), torch.empty_like(x)
+    _abi.check(_lib.attn_exp2_eval(_ptr(x), _ptr(yp), _ptr(yh), x.numel(), _stream(stream)), "attn_exp2_eval")
+    return yp, yh
+
+
+def attn_get_device_status(stream=None) -> int:
+    """Synchronises the stream; raises AttnError(ATTN_ERR_TIMEOUT) if a kernel recorded a failure."""
+    detail = ctypes.c_uint32(0)
+    st = _lib.attn_get_device_status(_stream(stream), ctypes.byref(detail))
+    if st != _abi.ATTN_OK:
+        raise AttnError(st, f"device status 0x{detail.value:08x}")
+    return detail.value
+
+
+class _Attention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, causal, softmax_scale, deterministic):
+        o, lse = attn_fwd(q, k, v, causal=causal, softmax_scale=softmax_scale)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.causal, ctx.scale, ctx.det = causal, softmax_scale, deterministic
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = attn_bwd(q, k, v, o, lse, do.contiguous(), causal=ctx.causal, softmax_scale=ctx.scale,
+                              deterministic=ctx.det)
+        return dq, dk, dv, None, None, None
+
+
+def attention(q, k, v, causal: bool = False, softmax_scale: Optional[float] = None, deterministic: bool = False):
+    """Autograd wrapper over attn_fwd / attn_bwd for [B, N, H, d] bf16 tensors."""
+    return _Attention.apply(q, k, v, causal, softmax_scale, deterministic)

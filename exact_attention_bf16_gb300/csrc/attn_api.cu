@@ -1,0 +1,364 @@
+// C-ABI entry points of libattn_gb300.so (declared in include/attn.h):
+// argument validation, TMA tensor-map encoding, workspace accounting and
+// kernel launches. All compute runs in the kernels of attn_fwd.cu and
+// attn_bwd.cu; this file holds host logic only.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "kernels.h"
+
+namespace gb300 {
+
+// Process-wide device status word (one copy per device that loads the library).
+__device__ uint32_t g_attn_status;
+
+namespace {
+
+thread_local char t_last_cuda_error[256] = "";
+
+attn_status_t cuda_fail(cudaError_t e, const char* what) {
+  std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "%s: %s", what, cudaGetErrorString(e));
+  return ATTN_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+std::mutex g_mu;
+
+// Device address of g_attn_status for the current device (looked up once per device).
+cudaError_t status_ptr(uint32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attn_status);
+    if (e != cudaSuccess) return e;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// TMA map over a bf16 tensor viewed as [n_b, n_rows, n_heads, d] with element
+// strides (sb, sn, sh) and unit stride on d. Box: 64 columns x 1 head x
+// `box_rows` rows x 1 batch, 128-byte swizzle (the UMMA K-major / MN-major
+// SW128 layout). Out-of-range rows read as zero.
+attn_status_t make_map(CUtensorMap* m, const void* base, int d, int n_heads, int64_t n_rows, int n_b, int64_t sb,
+                       int64_t sn, int64_t sh, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled unavailable");
+  // Size-1 dimensions may carry any stride; give them a valid one.
+  if (n_heads == 1) sh = d;
+  if (n_b == 1) sb = sn * (n_rows > 0 ? n_rows : 1);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n_heads),
+                        static_cast<cuuint64_t>(n_rows > 0 ? n_rows : 1), static_cast<cuuint64_t>(n_b)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(sh) * 2, static_cast<cuuint64_t>(sn) * 2,
+                           static_cast<cuuint64_t>(sb) * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "cuTensorMapEncodeTiled failed (%d)",
+                  static_cast<int>(r));
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool stride_ok(int64_t s) { return s >= 0 && (s % 8) == 0 && s < (int64_t(1) << 38); }
+
+bool supported_dims(int dqk, int dv) {
+  return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 128) || (dqk == 192 && dv == 128);
+}
+
+// Shape-level checks shared by every entry point.
+attn_status_t check_common(const attn_fwd_params* p, bool varlen) {
+  if (!p) return ATTN_ERR_INVALID_ARG;
+  if (!supported_dims(p->d_qk, p->d_v)) {
+    if (p->d_qk <= 0 || p->d_v <= 0) return ATTN_ERR_INVALID_ARG;
+    return ATTN_ERR_UNSUPPORTED;
+  }
+  if (p->heads < 1) return ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(p->softmax_scale) && p->softmax_scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (varlen) {
+    if (!p->cu_seqlens_q || !p->cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+    if (p->num_seqs < 1 || p->total_q < 0 || p->total_k < 0) return ATTN_ERR_INVALID_ARG;
+    if (p->max_seqlen_q < 0 || p->max_seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
+    if (p->max_seqlen_q > p->total_q || p->max_seqlen_k > p->total_k) return ATTN_ERR_INVALID_ARG;
+  } else {
+    if (p->cu_seqlens_q || p->cu_seqlens_k) return ATTN_ERR_INVALID_ARG;
+    if (p->batch < 1 || p->seqlen_q < 0 || p->seqlen_k < 0) return ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_OK;
+}
+
+attn_status_t check_tensor(const void* ptr, int64_t sb, int64_t sn, int64_t sh, bool varlen) {
+  if (!ptr || !aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
+  if (!stride_ok(sn) || !stride_ok(sh)) return ATTN_ERR_INVALID_ARG;
+  if (!varlen && !stride_ok(sb)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+#define ATTN_TRY(x)                        \
+  do {                                     \
+    attn_status_t _s = (x);                \
+    if (_s != ATTN_OK) return _s;          \
+  } while (0)
+
+attn_status_t check_fwd(const attn_fwd_params* p, bool varlen) {
+  ATTN_TRY(check_common(p, varlen));
+  ATTN_TRY(check_tensor(p->q, p->q_batch_stride, p->q_row_stride, p->q_head_stride, varlen));
+  ATTN_TRY(check_tensor(p->k, p->k_batch_stride, p->k_row_stride, p->k_head_stride, varlen));
+  ATTN_TRY(check_tensor(p->v, p->v_batch_stride, p->v_row_stride, p->v_head_stride, varlen));
+  ATTN_TRY(check_tensor(p->o, p->o_batch_stride, p->o_row_stride, p->o_head_stride, varlen));
+  if (!p->lse || (reinterpret_cast<uintptr_t>(p->lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream) {
+  ATTN_TRY(check_fwd(p, varlen));
+  const int nq_rows = varlen ? p->total_q : p->seqlen_q;
+  const int nk_rows = varlen ? p->total_k : p->seqlen_k;
+  const int units = varlen ? p->num_seqs : p->batch;
+  const int max_q = varlen ? p->max_seqlen_q : p->seqlen_q;
+  if (nq_rows == 0 || max_q == 0) return ATTN_OK;
+
+  FwdArgs a{};
+  a.o = p->o;
+  a.lse = p->lse;
+  a.o_sb = p->o_batch_stride;
+  a.o_sn = p->o_row_stride;
+  a.o_sh = p->o_head_stride;
+  a.batch = varlen ? 1 : p->batch;
+  a.heads = p->heads;
+  a.seqlen_q = varlen ? p->total_q : p->seqlen_q;
+  a.seqlen_k = varlen ? p->total_k : p->seqlen_k;
+  a.lse_sb = varlen ? 0 : static_cast<int64_t>(p->heads) * p->seqlen_q;
+  a.lse_sh = varlen ? p->total_q : p->seqlen_q;
+  a.cu_q = varlen ? p->cu_seqlens_q : nullptr;
+  a.cu_k = varlen ? p->cu_seqlens_k : nullptr;
+  a.num_units = units;
+  a.n_mblk = (max_q + 255) / 256;
+  a.scale_log2 = p->softmax_scale * 1.4426950408889634f;
+  a.causal = p->causal ? 1 : 0;
+  a.stats = p->rescale_stats;
+  cudaError_t e = status_ptr(&a.status);
+  if (e != cudaSuccess) return cuda_fail(e, "status word");
+
+  if (nk_rows == 0) {
+    // No keys anywhere: every row is empty. Dense and packed layouts both
+    // reduce to (units x heads x rows) with the strides above.
+    FwdArgs z = a;
+    if (varlen) {
+      z.num_units = 1;
+      z.seqlen_q = p->total_q;
+    }
+    e = launch_fwd_empty(z, p->d_v, stream);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "fwd empty launch");
+  }
+
+  const int nb = varlen ? 1 : p->batch;
+  CUtensorMap tq, tk, tv;
+  ATTN_TRY(make_map(&tq, p->q, p->d_qk, p->heads, nq_rows, nb, p->q_batch_stride, p->q_row_stride,
+                    p->q_head_stride, 128));
+  ATTN_TRY(make_map(&tk, p->k, p->d_qk, p->heads, nk_rows, nb, p->k_batch_stride, p->k_row_stride,
+                    p->k_head_stride, 128));
+  ATTN_TRY(make_map(&tv, p->v, p->d_v, p->heads, nk_rows, nb, p->v_batch_stride, p->v_row_stride,
+                    p->v_head_stride, 128));
+  e = launch_fwd(p->d_qk, p->d_v, tq, tk, tv, a, stream);
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "fwd launch");
+}
+
+
+int bwd_dkdv_rows(int d_qk) { return d_qk == 192 ? 64 : 128; }
+
+size_t bwd_workspace_bytes(const attn_bwd_params* p, bool varlen) {
+  const attn_fwd_params& f = p->fwd;
+  const int64_t rows = varlen ? static_cast<int64_t>(f.heads) * f.total_q
+                              : static_cast<int64_t>(f.batch) * f.heads * f.seqlen_q;
+  return static_cast<size_t>((rows * 4 + 255) / 256 * 256);
+}
+
+attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool varlen, cudaStream_t stream) {
+  if (!p) return ATTN_ERR_INVALID_ARG;
+  const attn_fwd_params& f = p->fwd;
+  ATTN_TRY(check_fwd(&f, varlen));
+  ATTN_TRY(check_tensor(p->dout, p->do_batch_stride, p->do_row_stride, p->do_head_stride, varlen));
+  ATTN_TRY(check_tensor(p->dq, p->dq_batch_stride, p->dq_row_stride, p->dq_head_stride, varlen));
+  ATTN_TRY(check_tensor(p->dk, p->dk_batch_stride, p->dk_row_stride, p->dk_head_stride, varlen));
+  ATTN_TRY(check_tensor(p->dv, p->dv_batch_stride, p->dv_row_stride, p->dv_head_stride, varlen));
+  const int nq_rows = varlen ? f.total_q : f.seqlen_q;
+  const int nk_rows = varlen ? f.total_k : f.seqlen_k;
+  const size_t need = bwd_workspace_bytes(p, varlen);
+  if (nq_rows > 0 && nk_rows > 0 && (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u)))
+    return ATTN_ERR_WORKSPACE;
+
+  BwdArgs a{};
+  a.o = f.o;
+  a.dout = p->dout;
+  a.lse = f.lse;
+  a.dsum = static_cast<float*>(ws);
+  a.dq = p->dq;
+  a.dk = p->dk;
+  a.dv = p->dv;
+  a.o_sb = f.o_batch_stride, a.o_sn = f.o_row_stride, a.o_sh = f.o_head_stride;
+  a.do_sb = p->do_batch_stride, a.do_sn = p->do_row_stride, a.do_sh = p->do_head_stride;
+  a.dq_sb = p->dq_batch_stride, a.dq_sn = p->dq_row_stride, a.dq_sh = p->dq_head_stride;
+  a.dk_sb = p->dk_batch_stride, a.dk_sn = p->dk_row_stride, a.dk_sh = p->dk_head_stride;
+  a.dv_sb = p->dv_batch_stride, a.dv_sn = p->dv_row_stride, a.dv_sh = p->dv_head_stride;
+  if (varlen) a.o_sb = a.do_sb = a.dq_sb = a.dk_sb = a.dv_sb = 0;
+  a.lse_sb = varlen ? 0 : static_cast<int64_t>(f.heads) * f.seqlen_q;
+  a.lse_sh = varlen ? f.total_q : f.seqlen_q;
+  a.batch = varlen ? 1 : f.batch;
+  a.heads = f.heads;
+  a.seqlen_q = nq_rows;
+  a.seqlen_k = nk_rows;
+  a.cu_q = varlen ? f.cu_seqlens_q : nullptr;
+  a.cu_k = varlen ? f.cu_seqlens_k : nullptr;
+  a.num_units = varlen ? f.num_seqs : f.batch;
+  const int max_q = varlen ? f.max_seqlen_q : f.seqlen_q;
+  const int max_k = varlen ? f.max_seqlen_k : f.seqlen_k;
+  a.n_qblk = (max_q + 127) / 128;
+  a.n_kblk = (max_k + 127) / 128;
+  a.scale = f.softmax_scale;
+  a.scale_log2 = f.softmax_scale * 1.4426950408889634f;
+  a.causal = f.causal ? 1 : 0;
+  cudaError_t e = status_ptr(&a.status);
+  if (e != cudaSuccess) return cuda_fail(e, "status word");
+
+  if (nq_rows == 0 || nk_rows == 0) {
+    // Nothing to differentiate through: no queries -> dK = dV = 0; no keys -> dQ = 0.
+    e = launch_bwd_zero(a, f.d_qk, f.d_v, nk_rows == 0, nq_rows == 0, stream);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "bwd zero launch");
+  }
+
+  const int nb = varlen ? 1 : f.batch;
+  const int qrows = bwd_dkdv_rows(f.d_qk);
+  CUtensorMap tq, tk, tv, tdo, tq2, tdo2;
+  ATTN_TRY(make_map(&tq, f.q, f.d_qk, f.heads, nq_rows, nb, f.q_batch_stride, f.q_row_stride, f.q_head_stride, 128));
+  ATTN_TRY(make_map(&tk, f.k, f.d_qk, f.heads, nk_rows, nb, f.k_batch_stride, f.k_row_stride, f.k_head_stride, 128));
+  ATTN_TRY(make_map(&tv, f.v, f.d_v, f.heads, nk_rows, nb, f.v_batch_stride, f.v_row_stride, f.v_head_stride, 128));
+  ATTN_TRY(make_map(&tdo, p->dout, f.d_v, f.heads, nq_rows, nb, p->do_batch_stride, p->do_row_stride,
+                    p->do_head_stride, 128));
+  ATTN_TRY(make_map(&tq2, f.q, f.d_qk, f.heads, nq_rows, nb, f.q_batch_stride, f.q_row_stride, f.q_head_stride,
+                    qrows));
+  ATTN_TRY(make_map(&tdo2, p->dout, f.d_v, f.heads, nq_rows, nb, p->do_batch_stride, p->do_row_stride,
+                    p->do_head_stride, qrows));
+  e = launch_bwd_preprocess(f.d_v, a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "bwd preprocess launch");
+  e = launch_bwd_dkdv(f.d_qk, f.d_v, tq2, tk, tv, tdo2, a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "bwd dkdv launch");
+  e = launch_bwd_dq(f.d_qk, f.d_v, tq, tk, tv, tdo, a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "bwd dq launch");
+  return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace gb300
+
+using namespace gb300;
+
+extern "C" {
+
+size_t attn_fwd_workspace_size(const attn_fwd_params* p) {
+  (void)p;
+  return 0;
+}
+
+attn_status_t attn_fwd(const attn_fwd_params* p, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  return run_fwd(p, false, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_varlen(const attn_fwd_params* p, void* workspace, size_t workspace_bytes,
+                              attn_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  return run_fwd(p, true, static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_bwd_workspace_size(const attn_bwd_params* p) {
+  if (!p) return 0;
+  return bwd_workspace_bytes(p, p->fwd.cu_seqlens_q != nullptr);
+}
+
+attn_status_t attn_bwd(const attn_bwd_params* p, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  return run_bwd(p, workspace, workspace_bytes, false, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_bwd_varlen(const attn_bwd_params* p, void* workspace, size_t workspace_bytes,
+                              attn_stream_t stream) {
+  return run_bwd(p, workspace, workspace_bytes, true, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_exp2_eval(const float* x, float* y_poly, float* y_hw, int64_t n, attn_stream_t stream) {
+  if (n < 0 || (n > 0 && !x) || (!y_poly && !y_hw)) return ATTN_ERR_INVALID_ARG;
+  cudaError_t e = launch_exp2_eval(x, y_poly, y_hw, n, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "exp2 eval launch");
+}
+
+attn_status_t attn_get_device_status(attn_stream_t stream, uint32_t* detail) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream sync");
+  uint32_t* d = nullptr;
+  e = status_ptr(&d);
+  if (e != cudaSuccess) return cuda_fail(e, "status word");
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, d, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (v != 0) {
+    const uint32_t zero = 0;
+    e = cudaMemcpy(d, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+  }
+  if (detail) *detail = v;
+  return v == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
+}
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+const char* attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+int32_t attn_abi_version(void) { return ATTN_ABI_VERSION; }
+size_t attn_fwd_params_size(void) { return sizeof(attn_fwd_params); }
+size_t attn_bwd_params_size(void) { return sizeof(attn_bwd_params); }
+
+}  // extern "C"

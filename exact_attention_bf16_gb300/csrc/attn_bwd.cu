@@ -1,0 +1,721 @@
+// Backward attention kernels for GB300 (sm_103a).
+//
+// Gradients of the loss <O, dO> (dQ, dK, dV; wittx "FlashAttention-4",
+// section 反向传播的优化) with P recomputed from the forward's LSE:
+//   P = 2^(scale*log2e * Q K^T - LSE*log2e),  dP = dO V^T,  D_i = dO_i . O_i,
+//   dS = P * (dP - D),  dV = P^T dO,  dK = scale * dS^T Q,  dQ = scale * dS K.
+//
+// Three launches:
+//   preprocess  D_i = sum_d dO_id O_id (fp32) into the workspace.
+//   dkdv        one CTA per 128-key tile (K, V stay in shared memory), looping
+//               over query tiles: S^T = K Q^T and dP^T = V dO^T into Tensor
+//               Memory, P^T / dS^T computed one key row per thread, then
+//               dV += P^T dO (P^T read straight from TMEM) and dK += dS^T Q
+//               with both accumulators resident in TMEM for the whole loop.
+//   dq          one CTA per 128-query tile (Q, dO stay in shared memory),
+//               looping over key tiles: S, dP, dS as above, dQ += dS K in TMEM.
+// Every output element is produced by exactly one CTA with a fixed summation
+// order, so results are bitwise reproducible run to run (the deterministic
+// mode costs nothing here). This trades the pages' single-pass design (dQ
+// partials reduced across CTAs with global atomics, or semaphore-ordered adds
+// in deterministic mode) for two extra GEMMs per tile pair (S and dP are
+// recomputed by the dq kernel) and no atomics at all.
+//
+// Roles: warps 0..7 are two softmax-gradient warpgroups (each TMEM lane =
+// one row, the two groups split the columns), warp 8 issues TMA copies,
+// warp 9 allocates TMEM and issues every tcgen05.mma from one thread.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx_sm100.cuh"
+
+namespace gb300 {
+namespace bwd {
+
+constexpr int KB = 128;          // keys per kv tile (TMEM lanes in dkdv)
+constexpr int MB = 128;          // queries per q tile in the dq kernel
+constexpr int kThreads = 320;    // 8 softmax warps + TMA warp + MMA warp
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kSoftThreads = 256;
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Stores 32 bf16 values (16 packed words) into row `row` of a K-major,
+// 128-byte-swizzled tile whose 64-column chunks are `chunk_bytes` apart,
+// starting at column col0 (a multiple of 32).
+__device__ __forceinline__ void st_swizzled_row32(uint8_t* tile, int chunk_bytes, int row, int col0,
+                                                  const uint32_t (&w)[16]) {
+  uint8_t* base = tile + (col0 / 64) * chunk_bytes + row * 128;
+  const int u0 = (col0 % 64) / 8;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int pu = (u0 + u) ^ (row & 7);
+    *reinterpret_cast<uint4*>(base + pu * 16) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+  }
+}
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&w)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) d[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+}
+
+// Sequence bounds of a work unit (dense: unit = batch index).
+struct Unit {
+  int b, q_start, k_start, nq, nk;
+};
+__device__ __forceinline__ Unit unit_bounds(const BwdArgs& a, int unit) {
+  Unit u{unit, 0, 0, a.seqlen_q, a.seqlen_k};
+  if (a.cu_q != nullptr) {
+    u.b = 0;
+    u.q_start = a.cu_q[unit];
+    u.nq = a.cu_q[unit + 1] - u.q_start;
+    u.k_start = a.cu_k[unit];
+    u.nk = a.cu_k[unit + 1] - u.k_start;
+  }
+  return u;
+}
+
+// ===========================================================================
+// Preprocess: D = rowsum(dO * O), one warp per (row, head).
+// ===========================================================================
+template <int DV>
+__global__ void preprocess_kernel(const BwdArgs a) {
+  const int64_t rows = static_cast<int64_t>(a.batch) * a.seqlen_q * a.heads;
+  const int64_t warp0 = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int64_t r = warp0; r < rows; r += nwarps) {
+    const int h = static_cast<int>(r % a.heads);
+    const int64_t bi = r / a.heads;
+    const int i = static_cast<int>(bi % a.seqlen_q);
+    const int b = static_cast<int>(bi / a.seqlen_q);
+    const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(a.o) + b * a.o_sb + i * a.o_sn + h * a.o_sh;
+    const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(a.dout) + b * a.do_sb + i * a.do_sn + h * a.do_sh;
+    float acc = 0.f;
+    for (int c = lane * 2; c < DV; c += 64) {
+      const __nv_bfloat162 ov = *reinterpret_cast<const __nv_bfloat162*>(o + c);
+      const __nv_bfloat162 gv = *reinterpret_cast<const __nv_bfloat162*>(g + c);
+      acc = fmaf(__bfloat162float(ov.x), __bfloat162float(gv.x), acc);
+      acc = fmaf(__bfloat162float(ov.y), __bfloat162float(gv.y), acc);
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) a.dsum[b * a.lse_sb + h * a.lse_sh + i] = acc;
+  }
+}
+
+// ===========================================================================
+// dK / dV kernel (key-stationary)
+// ===========================================================================
+template <int DQK, int DV>
+struct DkdvCfg {
+  static constexpr int QB = DQK == 192 ? 64 : 128;  // query rows per step (TMEM budget)
+  static constexpr int QCH = DQK / 64, VCH = DV / 64;
+  static constexpr int K_BYTES = QCH * KB * 128;
+  static constexpr int V_BYTES = VCH * KB * 128;
+  static constexpr int QT_BYTES = QCH * QB * 128;   // one query tile of Q
+  static constexpr int DOT_BYTES = VCH * QB * 128;  // one query tile of dO
+  static constexpr int NST = 2;
+  static constexpr int STAGE = QT_BYTES + DOT_BYTES;
+  static constexpr int DS_BYTES = (QB / 64) * KB * 128;  // dS^T [KB][QB] bf16, K-major
+  static constexpr int OFF_V = K_BYTES;
+  static constexpr int OFF_ST = OFF_V + V_BYTES;
+  static constexpr int OFF_DS = OFF_ST + NST * STAGE;
+  static constexpr int OFF_VEC = OFF_DS + DS_BYTES;          // [QB] LSE*log2e + [QB] D
+  static constexpr int OFF_BAR = OFF_VEC + 2 * QB * 4;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  // TMEM columns
+  static constexpr uint32_t tS = 0, tdP = QB, tdV = 2 * QB, tdK = 2 * QB + DV;
+  static_assert(tdK + DQK <= 512, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct DkdvBars {
+  uint64_t kv_full;
+  uint64_t st_full[2];
+  uint64_t st_empty[2];
+  uint64_t s_full;
+  uint64_t ds_full;
+  uint64_t acc_full;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+};
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo, const BwdArgs a) {
+  using C = DkdvCfg<DQK, DV>;
+  constexpr int QB = C::QB;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sST = smem + C::OFF_ST;
+  uint8_t* sDS = smem + C::OFF_DS;
+  float* sLSE = reinterpret_cast<float*>(smem + C::OFF_VEC);  // [QB]
+  float* sDv = sLSE + QB;                                      // [QB]
+  DkdvBars* bar = reinterpret_cast<DkdvBars*>(smem + C::OFF_BAR);
+
+  // heaviest key tiles first under the causal mask (tile 0 sees every query)
+  const int per = a.num_units * a.heads;
+  const int n = static_cast<int>(blockIdx.x) / per;
+  const int rem = static_cast<int>(blockIdx.x) % per;
+  const int h = rem % a.heads;
+  const Unit U = unit_bounds(a, rem / a.heads);
+  const int k0 = n * KB;
+  if (k0 >= U.nk) return;
+  int m_begin = 0;
+  if (a.causal) {
+    const int i_min = k0 - (U.nk - U.nq);  // first query row that sees key k0
+    m_begin = i_min > 0 ? i_min / QB : 0;
+  }
+  const int m_end = ceil_div(U.nq, QB);
+  const int T = m_end > m_begin ? m_end - m_begin : 0;
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    mbar_init(&bar->kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar->st_full[s], 1);
+      mbar_init(&bar->st_empty[s], 1);
+    }
+    mbar_init(&bar->s_full, 1);
+    mbar_init(&bar->ds_full, kSoftThreads);
+    mbar_init(&bar->acc_full, 1);
+    mbar_init(&bar->mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bar->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bar->tmem_base;
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar->kv_full, C::K_BYTES + C::V_BYTES);
+      for (int c = 0; c < C::QCH; ++c)
+        tma_load_4d(sK + c * KB * 128, &tmk, &bar->kv_full, c * 64, h, U.k_start + k0, U.b);
+      for (int c = 0; c < C::VCH; ++c)
+        tma_load_4d(sV + c * KB * 128, &tmv, &bar->kv_full, c * 64, h, U.k_start + k0, U.b);
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < T && ok; ++t) {
+        const int st = t % C::NST;
+        const uint32_t use = static_cast<uint32_t>(t / C::NST);
+        ok = mbar_wait(&bar->st_empty[st], (use & 1u) ^ 1u, a.status, 0x1100 + st);
+        if (!ok) break;
+        uint8_t* dst = sST + st * C::STAGE;
+        const int row = U.q_start + (m_begin + t) * QB;
+        mbar_arrive_expect_tx(&bar->st_full[st], C::STAGE);
+        for (int c = 0; c < C::QCH; ++c) tma_load_4d(dst + c * QB * 128, &tmq, &bar->st_full[st], c * 64, h, row, U.b);
+        for (int c = 0; c < C::VCH; ++c)
+          tma_load_4d(dst + C::QT_BYTES + c * QB * 128, &tmdo, &bar->st_full[st], c * 64, h, row, U.b);
+        ++issued;
+      }
+      if (!ok)
+        for (int t = issued - 1; t >= 0 && t >= issued - C::NST; --t)
+          mbar_wait(&bar->st_full[t % C::NST], static_cast<uint32_t>(t / C::NST) & 1u, nullptr, 0);
+      mbar_wait(&bar->kv_full, 0, nullptr, 0);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(KB, QB, false, false);  // S^T, dP^T: both operands K-major
+      constexpr uint32_t idV = idesc_bf16_f32(KB, DV, false, true);   // dV: B = dO, MN-major
+      constexpr uint32_t idK = idesc_bf16_f32(KB, DQK, false, true);  // dK: B = Q, MN-major
+      bool ok = mbar_wait(&bar->kv_full, 0, a.status, 0x1200);
+      const uint32_t kb = smem_u32(sK), vb = smem_u32(sV), dsb = smem_u32(sDS);
+      for (int t = 0; t < T && ok; ++t) {
+        const int st = t % C::NST;
+        ok = mbar_wait(&bar->st_full[st], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x1210);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qb = smem_u32(sST + st * C::STAGE);
+        const uint32_t gb = qb + C::QT_BYTES;
+        // S^T = K Q^T   (M = 128 keys, N = QB queries, K = d_qk)
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const uint64_t ad = smem_desc(kb + (kk / 4) * KB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
+          const uint64_t bd = smem_desc(qb + (kk / 4) * QB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
+          mma_ss(tbase + C::tS, ad, bd, idS, kk > 0 ? 1u : 0u);
+        }
+        // dP^T = V dO^T  (K = d_v)
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk) {
+          const uint64_t ad = smem_desc(vb + (kk / 4) * KB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
+          const uint64_t bd = smem_desc(gb + (kk / 4) * QB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
+          mma_ss(tbase + C::tdP, ad, bd, idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar->s_full);
+        ok = mbar_wait(&bar->ds_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1220);
+        if (!ok) break;
+        tc_fence_after();
+        // dV += P^T dO  (A = P^T from TMEM: 16 packed columns per 32-query chunk)
+#pragma unroll
+        for (int kk = 0; kk < QB / 16; ++kk) {
+          const uint64_t bd = smem_desc(gb + kk * 2048, QB * 128, 1024, SWZ_128B);
+          mma_ts(tbase + C::tdV, tbase + C::tS + (kk / 2) * 32 + (kk % 2) * 8, bd, idV, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        // dK += dS^T Q  (A = dS^T in shared memory, K-major)
+#pragma unroll
+        for (int kk = 0; kk < QB / 16; ++kk) {
+          const uint64_t ad = smem_desc(dsb + (kk / 4) * KB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
+          const uint64_t bd = smem_desc(qb + kk * 2048, QB * 128, 1024, SWZ_128B);
+          mma_ss(tbase + C::tdK, ad, bd, idK, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bar->st_empty[st]);
+      }
+      mma_commit(&bar->acc_full);
+      mma_commit(&bar->mma_done);
+      mbar_wait(&bar->mma_done, 0, a.status, 0x12ff);
+    }
+  } else {
+    // ================= softmax gradient: one key row per thread ============
+    const int wg = static_cast<int>(warp) / 4;           // which half of the query columns
+    const uint32_t quarter = warp & 3u;
+    const int j = static_cast<int>(quarter * 32 + lane);  // key row within the tile
+    const int kj = k0 + j;                                // key index within the sequence
+    const uint32_t lane_base = tbase + ((quarter * 32u) << 16);
+    // query rows i that see key kj: i >= i_vis (and kj < nk)
+    const int i_vis = a.causal ? kj - (U.nk - U.nq) : -0x40000000;
+    const bool key_ok = kj < U.nk;
+    const float sl2 = a.scale_log2;
+    constexpr int CPW = QB / 2;  // query columns per warpgroup
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int q0 = (m_begin + t) * QB;
+      {
+        const int tid = static_cast<int>(threadIdx.x);  // 0..255
+        named_bar_sync(1, kSoftThreads);  // everyone is done reading the previous step's vectors
+        if (tid < QB) {
+          const int i = q0 + tid;
+          float v = INFINITY;
+          if (i < U.nq) {
+            const float l = a.lse[U.b * a.lse_sb + h * a.lse_sh + U.q_start + i];
+            v = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+          }
+          sLSE[tid] = v;
+        } else if (tid < 2 * QB) {
+          const int i = q0 + tid - QB;
+          sDv[tid - QB] = (i < U.nq) ? a.dsum[U.b * a.lse_sb + h * a.lse_sh + U.q_start + i] : 0.f;
+        }
+        named_bar_sync(1, kSoftThreads);
+      }
+      ok = mbar_wait(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1300);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < CPW / 32; ++c) {
+        const int col0 = wg * CPW + c * 32;
+        uint32_t s[32], dp[32];
+        tmem_ld32(lane_base + C::tS + col0, s);
+        tmem_ld32(lane_base + C::tdP + col0, dp);
+        tmem_wait_ld();
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p[2], ds[2];
+#pragma unroll
+          for (int z = 0; z < 2; ++z) {
+            const int col = col0 + e + z;
+            const bool vis = key_ok && (q0 + col >= i_vis);
+            p[z] = vis ? ex2_mufu(fmaf(__uint_as_float(s[e + z]), sl2, -sLSE[col])) : 0.f;
+            ds[z] = p[z] * (__uint_as_float(dp[e + z]) - sDv[col]);
+          }
+          pw[e / 2] = pack_bf16x2(p[0], p[1]);
+          dw[e / 2] = pack_bf16x2(ds[0], ds[1]);
+        }
+        // P^T for these 32 queries goes to the first 16 columns of the S
+        // columns this thread just read (never into columns the other
+        // warpgroup has yet to read).
+        tmem_st16(lane_base + C::tS + col0, pw);
+        st_swizzled_row32(sDS, KB * 128, j, col0, dw);
+      }
+      tmem_wait_st();
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar->ds_full);
+    }
+    // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
+    if (ok && T > 0) {
+      ok = mbar_wait(&bar->acc_full, 0, a.status, 0x1310);
+      tc_fence_after();
+    }
+    const bool store = key_ok;
+    if (wg == 0) {
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dv) + U.b * a.dv_sb +
+                           static_cast<int64_t>(U.k_start + kj) * a.dv_sn + h * a.dv_sh;
+#pragma unroll
+      for (int c = 0; c < DV / 32; ++c) {
+        uint32_t v[32], w[16];
+        if (T > 0) {
+          tmem_ld32(lane_base + C::tdV + c * 32, v);
+          tmem_wait_ld();
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = T > 0 ? pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])) : 0u;
+        if (store) store_row_bf16(dst + c * 32, w);
+      }
+    } else {
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dk) + U.b * a.dk_sb +
+                           static_cast<int64_t>(U.k_start + kj) * a.dk_sn + h * a.dk_sh;
+#pragma unroll
+      for (int c = 0; c < DQK / 32; ++c) {
+        uint32_t v[32], w[16];
+        if (T > 0) {
+          tmem_ld32(lane_base + C::tdK + c * 32, v);
+          tmem_wait_ld();
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = T > 0 ? pack_bf16x2(__uint_as_float(v[2 * e]) * a.scale, __uint_as_float(v[2 * e + 1]) * a.scale)
+                       : 0u;
+        if (store) store_row_bf16(dst + c * 32, w);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tbase, 512);
+}
+
+// ===========================================================================
+// dQ kernel (query-stationary)
+// ===========================================================================
+template <int DQK, int DV>
+struct DqCfg {
+  static constexpr int QCH = DQK / 64, VCH = DV / 64;
+  static constexpr int Q_BYTES = QCH * MB * 128;
+  static constexpr int DO_BYTES = VCH * MB * 128;
+  static constexpr int K_BYTES = QCH * KB * 128;
+  static constexpr int V_BYTES = VCH * KB * 128;
+  static constexpr int NST = DQK == 192 ? 1 : 2;
+  static constexpr int STAGE = K_BYTES + V_BYTES;
+  static constexpr int DS_BYTES = 2 * MB * 128;  // dS [MB][KB] bf16, K-major
+  static constexpr int OFF_DO = Q_BYTES;
+  static constexpr int OFF_ST = OFF_DO + DO_BYTES;
+  static constexpr int OFF_DS = OFF_ST + NST * STAGE;
+  static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static constexpr uint32_t tS = 0, tdP = 128, tdQ = 256;
+  static_assert(tdQ + DQK <= 512, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct DqBars {
+  uint64_t q_full;
+  uint64_t st_full[2];
+  uint64_t st_empty[2];
+  uint64_t s_full;
+  uint64_t ds_full;
+  uint64_t acc_full;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ int key_limit(int row, int nq, int nk, int causal) {
+  if (!causal) return nk;
+  int lim = row + (nk - nq) + 1;
+  return lim < 0 ? 0 : (lim > nk ? nk : lim);
+}
+
+template <int DQK, int DV>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+              const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo, const BwdArgs a) {
+  using C = DqCfg<DQK, DV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sdO = smem + C::OFF_DO;
+  uint8_t* sST = smem + C::OFF_ST;
+  uint8_t* sDS = smem + C::OFF_DS;
+  DqBars* bar = reinterpret_cast<DqBars*>(smem + C::OFF_BAR);
+
+  const int per = a.num_units * a.heads;
+  const int m = a.n_qblk - 1 - static_cast<int>(blockIdx.x) / per;  // heaviest (last) query tiles first
+  const int rem = static_cast<int>(blockIdx.x) % per;
+  const int h = rem % a.heads;
+  const Unit U = unit_bounds(a, rem / a.heads);
+  const int q0 = m * MB;
+  if (q0 >= U.nq) return;
+  const int last = min(q0 + MB - 1, U.nq - 1);
+  const int T = ceil_div(key_limit(last, U.nq, U.nk, a.causal), KB);
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    mbar_init(&bar->q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar->st_full[s], 1);
+      mbar_init(&bar->st_empty[s], 1);
+    }
+    mbar_init(&bar->s_full, 1);
+    mbar_init(&bar->ds_full, kSoftThreads);
+    mbar_init(&bar->acc_full, 1);
+    mbar_init(&bar->mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bar->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bar->tmem_base;
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar->q_full, C::Q_BYTES + C::DO_BYTES);
+      for (int c = 0; c < C::QCH; ++c)
+        tma_load_4d(sQ + c * MB * 128, &tmq, &bar->q_full, c * 64, h, U.q_start + q0, U.b);
+      for (int c = 0; c < C::VCH; ++c)
+        tma_load_4d(sdO + c * MB * 128, &tmdo, &bar->q_full, c * 64, h, U.q_start + q0, U.b);
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < T && ok; ++t) {
+        const int st = t % C::NST;
+        const uint32_t use = static_cast<uint32_t>(t / C::NST);
+        ok = mbar_wait(&bar->st_empty[st], (use & 1u) ^ 1u, a.status, 0x2100 + st);
+        if (!ok) break;
+        uint8_t* dst = sST + st * C::STAGE;
+        const int row = U.k_start + t * KB;
+        mbar_arrive_expect_tx(&bar->st_full[st], C::STAGE);
+        for (int c = 0; c < C::QCH; ++c) tma_load_4d(dst + c * KB * 128, &tmk, &bar->st_full[st], c * 64, h, row, U.b);
+        for (int c = 0; c < C::VCH; ++c)
+          tma_load_4d(dst + C::K_BYTES + c * KB * 128, &tmv, &bar->st_full[st], c * 64, h, row, U.b);
+        ++issued;
+      }
+      if (!ok)
+        for (int t = issued - 1; t >= 0 && t >= issued - C::NST; --t)
+          mbar_wait(&bar->st_full[t % C::NST], static_cast<uint32_t>(t / C::NST) & 1u, nullptr, 0);
+      mbar_wait(&bar->q_full, 0, nullptr, 0);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(MB, KB, false, false);
+      constexpr uint32_t idQ = idesc_bf16_f32(MB, DQK, false, true);  // B = K tile, MN-major
+      bool ok = mbar_wait(&bar->q_full, 0, a.status, 0x2200);
+      const uint32_t qb = smem_u32(sQ), gb = smem_u32(sdO), dsb = smem_u32(sDS);
+      for (int t = 0; t < T && ok; ++t) {
+        const int st = t % C::NST;
+        ok = mbar_wait(&bar->st_full[st], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x2210);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(sST + st * C::STAGE);
+        const uint32_t vb = kb + C::K_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {  // S = Q K^T
+          const uint32_t off = (kk / 4) * MB * 128 + (kk % 4) * 32;
+          mma_ss(tbase + C::tS, smem_desc(qb + off, 16, 1024, SWZ_128B), smem_desc(kb + off, 16, 1024, SWZ_128B), idS,
+                 kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < DV / 16; ++kk) {  // dP = dO V^T
+          const uint32_t off = (kk / 4) * MB * 128 + (kk % 4) * 32;
+          mma_ss(tbase + C::tdP, smem_desc(gb + off, 16, 1024, SWZ_128B), smem_desc(vb + off, 16, 1024, SWZ_128B),
+                 idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar->s_full);
+        ok = mbar_wait(&bar->ds_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2220);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < KB / 16; ++kk) {  // dQ += dS K   (B = K tile as [d][kv], MN-major)
+          const uint64_t ad = smem_desc(dsb + (kk / 4) * MB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
+          const uint64_t bd = smem_desc(kb + kk * 2048, KB * 128, 1024, SWZ_128B);
+          mma_ss(tbase + C::tdQ, ad, bd, idQ, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bar->st_empty[st]);
+      }
+      mma_commit(&bar->acc_full);
+      mma_commit(&bar->mma_done);
+      mbar_wait(&bar->mma_done, 0, a.status, 0x22ff);
+    }
+  } else {
+    // ================= softmax gradient: one query row per thread ==========
+    const int wg = static_cast<int>(warp) / 4;
+    const uint32_t quarter = warp & 3u;
+    const int r = static_cast<int>(quarter * 32 + lane);  // query row within the tile
+    const int i = q0 + r;
+    const uint32_t lane_base = tbase + ((quarter * 32u) << 16);
+    const int lim = key_limit(i, U.nq, U.nk, a.causal);
+    float lse2 = INFINITY, dsum = 0.f;
+    if (i < U.nq) {
+      const float l = a.lse[U.b * a.lse_sb + h * a.lse_sh + U.q_start + i];
+      lse2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+      dsum = a.dsum[U.b * a.lse_sb + h * a.lse_sh + U.q_start + i];
+    }
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      ok = mbar_wait(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2300);
+      if (!ok) break;
+      tc_fence_after();
+      const int cnt = lim - t * KB;  // visible keys of this row in tile t
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = wg * 64 + c * 32;
+        uint32_t s[32], dp[32];
+        tmem_ld32(lane_base + C::tS + col0, s);
+        tmem_ld32(lane_base + C::tdP + col0, dp);
+        tmem_wait_ld();
+        uint32_t dw[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float ds[2];
+#pragma unroll
+          for (int z = 0; z < 2; ++z) {
+            const bool vis = col0 + e + z < cnt;
+            const float p = vis ? ex2_mufu(fmaf(__uint_as_float(s[e + z]), sl2, -lse2)) : 0.f;
+            ds[z] = p * (__uint_as_float(dp[e + z]) - dsum);
+          }
+          dw[e / 2] = pack_bf16x2(ds[0], ds[1]);
+        }
+        st_swizzled_row32(sDS, MB * 128, r, col0, dw);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar->ds_full);
+    }
+    if (ok && T > 0) {
+      ok = mbar_wait(&bar->acc_full, 0, a.status, 0x2310);
+      tc_fence_after();
+    }
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + U.b * a.dq_sb +
+                         static_cast<int64_t>(U.q_start + i) * a.dq_sn + h * a.dq_sh;
+    constexpr int CPW = DQK / 2;  // dQ columns per warpgroup (32, 64 or 96)
+#pragma unroll
+    for (int c = 0; c < CPW / 32; ++c) {
+      const int col0 = wg * CPW + c * 32;
+      uint32_t v[32], w[16];
+      if (T > 0) {
+        tmem_ld32(lane_base + C::tdQ + col0, v);
+        tmem_wait_ld();
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        w[e] = T > 0 ? pack_bf16x2(__uint_as_float(v[2 * e]) * a.scale, __uint_as_float(v[2 * e + 1]) * a.scale) : 0u;
+      if (i < U.nq) store_row_bf16(dst + col0, w);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tbase, 512);
+}
+
+// Zero rows: dQ (all queries) and/or dK, dV (all keys).
+__global__ void zero_kernel(void* base, int64_t sb, int64_t sn, int64_t sh, int nb, int nrows, int heads, int d) {
+  const int64_t total = static_cast<int64_t>(nb) * nrows * heads;
+  for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; r < total;
+       r += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int h = static_cast<int>(r % heads);
+    const int64_t bi = r / heads;
+    const int i = static_cast<int>(bi % nrows);
+    const int b = static_cast<int>(bi / nrows);
+    __nv_bfloat16* p = static_cast<__nv_bfloat16*>(base) + b * sb + i * sn + h * sh;
+    for (int c = 0; c < d; ++c) p[c] = __float2bfloat16_rn(0.f);
+  }
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int DQK, int DV>
+cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                          const BwdArgs& a, cudaStream_t stream) {
+  using C = DkdvCfg<DQK, DV>;
+  auto kern = dkdv_kernel<DQK, DV>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(kern, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int64_t grid = static_cast<int64_t>(a.n_kblk) * a.num_units * a.heads;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
+}
+
+template <int DQK, int DV>
+cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                        const BwdArgs& a, cudaStream_t stream) {
+  using C = DqCfg<DQK, DV>;
+  auto kern = dq_kernel<DQK, DV>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(kern, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int64_t grid = static_cast<int64_t>(a.n_qblk) * a.num_units * a.heads;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
+}
+
+}  // namespace bwd
+
+int bwd_dkdv_query_rows(int d_qk) { return d_qk == 192 ? 64 : 128; }
+
+cudaError_t launch_bwd_preprocess(int d_v, const BwdArgs& a, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(a.batch) * a.seqlen_q * a.heads;
+  if (rows == 0) return cudaSuccess;
+  const int64_t blocks = (rows * 32 + 255) / 256 < 16384 ? (rows * 32 + 255) / 256 : 16384;
+  if (d_v == 64) bwd::preprocess_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  else if (d_v == 128) bwd::preprocess_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+  if (d_qk == 64 && d_v == 64) return bwd::launch_dkdv_t<64, 64>(tq, tk, tv, tdo, a, stream);
+  if (d_qk == 128 && d_v == 128) return bwd::launch_dkdv_t<128, 128>(tq, tk, tv, tdo, a, stream);
+  if (d_qk == 192 && d_v == 128) return bwd::launch_dkdv_t<192, 128>(tq, tk, tv, tdo, a, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_dq(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+  if (d_qk == 64 && d_v == 64) return bwd::launch_dq_t<64, 64>(tq, tk, tv, tdo, a, stream);
+  if (d_qk == 128 && d_v == 128) return bwd::launch_dq_t<128, 128>(tq, tk, tv, tdo, a, stream);
+  if (d_qk == 192 && d_v == 128) return bwd::launch_dq_t<192, 128>(tq, tk, tv, tdo, a, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_zero(const BwdArgs& a, int d_qk, int d_v, bool zero_dq, bool zero_dkdv, cudaStream_t stream) {
+  auto go = [&](void* p, int64_t sb, int64_t sn, int64_t sh, int nrows, int d) -> cudaError_t {
+    const int64_t total = static_cast<int64_t>(a.batch) * nrows * a.heads;
+    if (total == 0) return cudaSuccess;
+    const int blocks = static_cast<int>(total / 256 + 1 < 4096 ? total / 256 + 1 : 4096);
+    bwd::zero_kernel<<<blocks, 256, 0, stream>>>(p, sb, sn, sh, a.batch, nrows, a.heads, d);
+    return cudaGetLastError();
+  };
+  cudaError_t e = cudaSuccess;
+  if (zero_dq) e = go(a.dq, a.dq_sb, a.dq_sn, a.dq_sh, a.seqlen_q, d_qk);
+  if (e == cudaSuccess && zero_dkdv) e = go(a.dk, a.dk_sb, a.dk_sn, a.dk_sh, a.seqlen_k, d_qk);
+  if (e == cudaSuccess && zero_dkdv) e = go(a.dv, a.dv_sb, a.dv_sn, a.dv_sh, a.seqlen_k, d_v);
+  return e;
+}
+
+}  // namespace gb300

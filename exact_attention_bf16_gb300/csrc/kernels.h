@@ -1,0 +1,74 @@
+// Internal interface between the C-ABI layer (attn_api.cu) and the kernel
+// translation units. Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace gb300 {
+
+// Forward kernel arguments (passed by value; tensor maps go separately as
+// __grid_constant__ parameters).
+struct FwdArgs {
+  void* o;                 // bf16 output
+  float* lse;              // fp32 output
+  int64_t o_sb, o_sn, o_sh;  // element strides of O (batch, row, head)
+  int64_t lse_sb, lse_sh;    // element strides of LSE (batch, head); row stride 1
+  int batch, heads, seqlen_q, seqlen_k;
+  const int* cu_q;           // varlen offsets (device) or nullptr for dense
+  const int* cu_k;
+  int num_units;             // batch (dense) or number of sequences (varlen)
+  int n_mblk;                // 256-row query blocks per unit = ceil(max_seqlen_q / 256)
+  float scale_log2;          // softmax_scale * log2(e)
+  int causal;
+  uint32_t* status;          // device status word
+  unsigned long long* stats; // optional rescale counters
+};
+
+cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& a, cudaStream_t stream);
+
+// Fills O = 0 and LSE = -inf for rows that see no key at all (Nk == 0).
+cudaError_t launch_fwd_empty(const FwdArgs& a, int d_v, cudaStream_t stream);
+
+// Backward kernel arguments. Dense tensors are [B, N, H, d]; varlen packed
+// [total, H, d] with cu_q / cu_k offsets (batch = 1 then).
+struct BwdArgs {
+  const void* o;             // forward output (bf16), read by the preprocess step
+  const void* dout;          // incoming gradient dO (bf16)
+  const float* lse;          // forward LSE (natural log), same layout as FwdArgs
+  float* dsum;               // workspace: D_i = dO_i . O_i (fp32), LSE layout
+  void* dq;                  // outputs (bf16)
+  void* dk;
+  void* dv;
+  int64_t o_sb, o_sn, o_sh;
+  int64_t do_sb, do_sn, do_sh;
+  int64_t dq_sb, dq_sn, dq_sh;
+  int64_t dk_sb, dk_sn, dk_sh;
+  int64_t dv_sb, dv_sn, dv_sh;
+  int64_t lse_sb, lse_sh;
+  int batch, heads, seqlen_q, seqlen_k;  // varlen: seqlen_* = total rows
+  const int* cu_q;
+  const int* cu_k;
+  int num_units;
+  int n_qblk;        // q tiles per unit for the dQ kernel: ceil(max_seqlen_q / 128)
+  int n_kblk;        // kv tiles per unit for the dK/dV kernel: ceil(max_seqlen_k / 128)
+  float scale;       // softmax_scale
+  float scale_log2;  // softmax_scale * log2(e)
+  int causal;
+  uint32_t* status;
+};
+
+// D = rowsum(dO * O) into args.dsum.
+cudaError_t launch_bwd_preprocess(int d_v, const BwdArgs& a, cudaStream_t stream);
+// dK, dV (KV-stationary) and dQ (Q-stationary). Maps: q, k, v, dO.
+cudaError_t launch_bwd_dkdv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dq(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+// Zero-fills dQ, dK, dV rows of a problem with no keys or no queries.
+cudaError_t launch_bwd_zero(const BwdArgs& a, int d_qk, int d_v, bool zero_dq, bool zero_dkdv, cudaStream_t stream);
+
+cudaError_t launch_exp2_eval(const float* x, float* y_poly, float* y_hw, int64_t n, cudaStream_t stream);
+
+}  // namespace gb300

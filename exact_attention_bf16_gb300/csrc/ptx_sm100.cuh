@@ -76,6 +76,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (i > 64) __nanosleep(64);
+    // Another role or CTA already failed: stop waiting early (legitimate
+    // waits here last microseconds, never 2^16 polls).
+    if ((i & 0xFFFu) == 0xFFFu && i > (1u << 16) && status && *reinterpret_cast<volatile uint32_t*>(status) != 0)
+      return false;
   }
   record_error(status, DEV_TIMEOUT_MBAR, where);
   return false;

@@ -1,0 +1,175 @@
+/*
+ * attn.h — C ABI of libattn_gb300.so: exact fused scaled-dot-product
+ * attention in bf16 for NVIDIA GB300 (sm_103a), forward and backward.
+ *
+ * What is computed (all entry points): for every (batch or sequence, head),
+ *   a_ij  = softmax_scale * q_i . k_j        for visible keys j, -inf otherwise
+ *   O_i   = sum_j softmax_j(a_i) v_j,        LSE_i = log sum_j exp(a_ij)
+ * and, in the backward entry points, the gradients of <O, dO>:
+ *   P = exp(a - LSE), dV = P^T dO, dP = dO V^T, D_i = dO_i . O_i,
+ *   dS = P * (dP - D), dQ = scale * dS K, dK = scale * dS^T Q.
+ * This is exact attention; the tiled online softmax that computes it is the
+ * one of the FlashAttention series (ainexis deep-dive "Tri Dao
+ * FlashAttention-4", section 背景), with the conditional rescaling of wittx
+ * "FlashAttention-4", section 90%的rescaling都是白干的 (rescale only when a
+ * row's max grows by more than 8.0 in log2 units, exact final normalisation),
+ * and exp2 split between the hardware unit and a Cody-Waite + cubic polynomial
+ * on the FMA pipe (same page, section 用软件"伪造"硬件指令).
+ *
+ * Visibility. Key j (of a sequence of Nk keys) is visible to query i (of Nq
+ * queries) iff j < Nk and, when causal != 0, j <= i + (Nk - Nq) (causal mask
+ * aligned to the bottom-right corner; equals j <= i when Nq == Nk). A query
+ * row that sees no key gets O = 0, LSE = -inf and zero gradient.
+ *
+ * Layouts (all element counts, not bytes). Dense tensors are 4-D
+ * [batch, seqlen, heads, head_dim] addressed as
+ *   base + b*batch_stride + n*row_stride + h*head_stride + d,
+ * i.e. head_dim must be contiguous. Variable-length ("varlen") tensors are
+ * packed [total_tokens, heads, head_dim]: the batch stride is ignored and
+ * sequence s occupies rows cu_seqlens[s] .. cu_seqlens[s+1]-1.
+ * LSE is fp32, natural log, contiguous [batch, heads, seqlen_q] (dense) or
+ * [heads, total_q] (varlen).
+ *
+ * Requirements (else ATTN_ERR_INVALID_ARG, nothing launched):
+ *   - (d_qk, d_v) in {(64,64), (128,128), (192,128)}  (else ATTN_ERR_UNSUPPORTED);
+ *   - q, k, v, o, dO, dQ, dK, dV base addresses 16-byte aligned, every stride a
+ *     multiple of 8 elements (16 bytes), lse 4-byte aligned;
+ *   - softmax_scale finite and > 0; batch, heads >= 1; seqlens >= 0.
+ *
+ * Ownership and execution. Every pointer in the parameter structs is a
+ * DEVICE pointer owned by the caller; the library never allocates, frees or
+ * keeps a pointer after the call returns. Scratch memory ("workspace") is
+ * passed in by the caller: query its size with the *_workspace_size call;
+ * a workspace may be reused by calls that are ordered on the same stream but
+ * must not be shared by calls that can run concurrently. Calls are
+ * asynchronous on `stream`: a return of ATTN_OK means the work was enqueued.
+ * Kernel-side failures (a bounded wait that gave up) are recorded in a
+ * per-process device status word, read (and cleared) by
+ * attn_get_device_status. All entry points are thread-safe for distinct
+ * output buffers.
+ */
+#ifndef ATTN_GB300_H_
+#define ATTN_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_ABI_VERSION 1
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* bad pointer, size, stride, alignment or scale */
+  ATTN_ERR_UNSUPPORTED = 2,  /* head-dim combination not built */
+  ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed (see attn_last_cuda_error) */
+  ATTN_ERR_TIMEOUT = 4,      /* a kernel's bounded wait gave up (device status word) */
+  ATTN_ERR_WORKSPACE = 5     /* workspace missing or smaller than *_workspace_size */
+} attn_status_t;
+
+/* Opaque CUDA stream handle (cudaStream_t); NULL is the legacy default stream. */
+typedef void* attn_stream_t;
+
+/* Forward parameters. Inputs q, k, v (bf16); outputs o (bf16) and lse (fp32).
+ * Dense: batch, seqlen_q, seqlen_k describe [batch, seqlen, heads, d] tensors
+ * and cu_seqlens_q / cu_seqlens_k must be NULL. Varlen: cu_seqlens_q and
+ * cu_seqlens_k are device int32 arrays of num_seqs+1 non-decreasing offsets
+ * starting at 0; total_q / total_k are the packed row counts (= last offset),
+ * max_seqlen_q / max_seqlen_k bound every sequence's length; batch and the
+ * batch strides are ignored. */
+typedef struct attn_fwd_params {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int64_t q_batch_stride, q_row_stride, q_head_stride;
+  int64_t k_batch_stride, k_row_stride, k_head_stride;
+  int64_t v_batch_stride, v_row_stride, v_head_stride;
+  int64_t o_batch_stride, o_row_stride, o_head_stride;
+  int32_t batch;
+  int32_t heads;
+  int32_t seqlen_q;
+  int32_t seqlen_k;
+  int32_t d_qk;
+  int32_t d_v;
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  int32_t num_seqs;
+  int32_t max_seqlen_q;
+  int32_t max_seqlen_k;
+  int32_t total_q;
+  int32_t total_k;
+  float softmax_scale;
+  int32_t causal;
+  int32_t reserved0;
+  /* Optional (may be NULL): device uint64[2] to which the forward kernel adds
+   * the number of conditional rescales performed after a row's first key
+   * tile ([0]) and the number of such rescale opportunities ([1]). */
+  unsigned long long* rescale_stats;
+} attn_fwd_params;
+
+/* Backward parameters. `fwd` holds q, k, v, the forward's outputs o and lse
+ * (read-only here), shapes, scale and mask; dout is the incoming gradient dO
+ * (bf16, same layout rules as o); dq, dk, dv (bf16) are written. With
+ * deterministic != 0 the dQ reduction runs in a fixed order and repeated calls
+ * on identical inputs give bitwise-identical dq/dk/dv on the same device. */
+typedef struct attn_bwd_params {
+  attn_fwd_params fwd;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  int64_t do_batch_stride, do_row_stride, do_head_stride;
+  int64_t dq_batch_stride, dq_row_stride, dq_head_stride;
+  int64_t dk_batch_stride, dk_row_stride, dk_head_stride;
+  int64_t dv_batch_stride, dv_row_stride, dv_head_stride;
+  int32_t deterministic;
+  int32_t reserved0;
+} attn_bwd_params;
+
+/* Bytes of device workspace the matching call needs (0 means none: pass NULL). */
+size_t attn_fwd_workspace_size(const attn_fwd_params* p);
+size_t attn_bwd_workspace_size(const attn_bwd_params* p);
+
+/* Dense forward: O, LSE from Q, K, V. */
+attn_status_t attn_fwd(const attn_fwd_params* p, void* workspace, size_t workspace_bytes, attn_stream_t stream);
+/* Variable-length forward (cu_seqlens_q / cu_seqlens_k required). */
+attn_status_t attn_fwd_varlen(const attn_fwd_params* p, void* workspace, size_t workspace_bytes,
+                              attn_stream_t stream);
+/* Dense backward: dQ, dK, dV from Q, K, V, O, LSE, dO. */
+attn_status_t attn_bwd(const attn_bwd_params* p, void* workspace, size_t workspace_bytes, attn_stream_t stream);
+/* Variable-length backward. */
+attn_status_t attn_bwd_varlen(const attn_bwd_params* p, void* workspace, size_t workspace_bytes,
+                              attn_stream_t stream);
+
+/* Diagnostic: evaluates the kernels' two exp2 paths on n device floats x:
+ * y_poly = Cody-Waite split + cubic on the FMA pipe (NULL to skip),
+ * y_hw = the hardware ex2 approximation (NULL to skip). Same code as the
+ * forward kernel's softmax uses (wittx "FlashAttention-4", section
+ * 用软件"伪造"硬件指令). */
+attn_status_t attn_exp2_eval(const float* x, float* y_poly, float* y_hw, int64_t n, attn_stream_t stream);
+
+/* Synchronises `stream`, then returns ATTN_OK if no kernel recorded a
+ * failure since the last call, else ATTN_ERR_TIMEOUT (the word is cleared).
+ * If detail != NULL it receives the raw status word (code << 24 | site). */
+attn_status_t attn_get_device_status(attn_stream_t stream, uint32_t* detail);
+
+/* Human-readable name of a status code (static storage). */
+const char* attn_status_string(attn_status_t s);
+
+/* Last CUDA error string seen by the library on this thread ("" if none). */
+const char* attn_last_cuda_error(void);
+
+/* ABI checks for bindings: ATTN_ABI_VERSION and sizeof of the parameter structs. */
+int32_t attn_abi_version(void);
+size_t attn_fwd_params_size(void);
+size_t attn_bwd_params_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H_ */

@@ -1,0 +1,120 @@
+"""The C-ABI library loads, exports every entry point include/attn.h declares,
+agrees with the binding on struct layout, and rejects bad arguments before
+touching the GPU. CPU only (no kernel is launched)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import __graft_entry__
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    from exact_attention_bf16_gb300 import _abi as abi
+    return abi.load()
+
+
+@pytest.fixture(scope="module")
+def _abi(lib):
+    from exact_attention_bf16_gb300 import _abi as abi
+    return abi
+
+
+def declared_functions():
+    import os
+    text = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("attn_fwd", "attn_fwd_varlen", "attn_bwd", "attn_bwd_varlen", "attn_fwd_workspace_size",
+                 "attn_bwd_workspace_size", "attn_get_device_status", "attn_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib, _abi):
+    out = subprocess.run(["nm", "-D", "--defined-only", _abi.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\sT\s(attn_[a-z0-9_]+)$", out, flags=re.M))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_struct_layout_and_version(lib, _abi):
+    assert lib.attn_abi_version() == _abi.ABI_VERSION
+    assert lib.attn_fwd_params_size() == ctypes.sizeof(_abi.AttnFwdParams)
+    assert lib.attn_bwd_params_size() == ctypes.sizeof(_abi.AttnBwdParams)
+
+
+def test_status_strings(lib, _abi):
+    for code, name in _abi.STATUS.items():
+        assert lib.attn_status_string(code).decode() == name
+
+
+def _valid_fwd(_abi):
+    p = _abi.AttnFwdParams()
+    fake = 0x10000  # 16-byte aligned non-null dummy; never dereferenced by the checks below
+    p.q = p.k = p.v = p.o = p.lse = fake
+    for t in "qkvo":
+        setattr(p, f"{t}_batch_stride", 128 * 4 * 64)
+        setattr(p, f"{t}_row_stride", 4 * 64)
+        setattr(p, f"{t}_head_stride", 64)
+    p.batch, p.heads, p.seqlen_q, p.seqlen_k, p.d_qk, p.d_v = 1, 4, 128, 128, 64, 64
+    p.softmax_scale = 0.125
+    return p
+
+
+INVALID, UNSUPPORTED = 1, 2
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda p: setattr(p, "d_qk", 96), UNSUPPORTED),
+    (lambda p: (setattr(p, "d_qk", 128), setattr(p, "d_v", 64)), UNSUPPORTED),
+    (lambda p: setattr(p, "d_qk", 0), INVALID),
+    (lambda p: setattr(p, "softmax_scale", 0.0), INVALID),
+    (lambda p: setattr(p, "softmax_scale", float("nan")), INVALID),
+    (lambda p: setattr(p, "softmax_scale", -1.0), INVALID),
+    (lambda p: setattr(p, "heads", 0), INVALID),
+    (lambda p: setattr(p, "batch", 0), INVALID),
+    (lambda p: setattr(p, "seqlen_q", -1), INVALID),
+    (lambda p: setattr(p, "q", 0x10008), INVALID),       # misaligned
+    (lambda p: setattr(p, "k", None), INVALID),           # null
+    (lambda p: setattr(p, "v_row_stride", 4 * 64 + 4), INVALID),  # not a multiple of 8
+    (lambda p: setattr(p, "lse", 0x10002), INVALID),
+    (lambda p: setattr(p, "cu_seqlens_q", 0x10000), INVALID),  # dense call with offsets
+])
+def test_fwd_rejects_bad_arguments_without_a_gpu(lib, _abi, mutate, expect):
+    p = _valid_fwd(_abi)
+    mutate(p)
+    assert lib.attn_fwd(ctypes.byref(p), None, 0, None) == expect
+
+
+def test_varlen_requires_offsets(lib, _abi):
+    p = _valid_fwd(_abi)
+    p.num_seqs, p.total_q, p.total_k, p.max_seqlen_q, p.max_seqlen_k = 1, 128, 128, 128, 128
+    assert lib.attn_fwd_varlen(ctypes.byref(p), None, 0, None) == _abi.ATTN_ERR_INVALID_ARG
+    p.cu_seqlens_q = p.cu_seqlens_k = 0x10000
+    p.max_seqlen_q = 129  # longer than the packed batch
+    assert lib.attn_fwd_varlen(ctypes.byref(p), None, 0, None) == _abi.ATTN_ERR_INVALID_ARG
+
+
+def test_null_params(lib, _abi):
+    assert lib.attn_fwd(None, None, 0, None) == _abi.ATTN_ERR_INVALID_ARG
+    assert lib.attn_bwd(None, None, 0, None) == _abi.ATTN_ERR_INVALID_ARG
+    assert lib.attn_exp2_eval(None, None, None, 4, None) == _abi.ATTN_ERR_INVALID_ARG
+
+
+def test_product_path_does_not_import_the_oracle(_abi):
+    pkg = os.path.dirname(_abi.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(root, f), encoding="utf-8").read()
+                assert "oracle" not in src.replace("CPU oracle", ""), f

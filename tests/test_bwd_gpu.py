@@ -1,0 +1,171 @@
+"""Backward parity of the CUDA path (through the C ABI) against the fp64 CPU
+oracle, plus bitwise reproducibility of the deterministic mode."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import attention_bwd
+from parity import check_grads
+
+pytestmark = pytest.mark.gpu
+
+DIMS = [(64, 64), (128, 128), (192, 128)]
+
+
+@pytest.fixture(scope="module")
+def ea():
+    import exact_attention_bf16_gb300 as ea
+    return ea
+
+
+def gpu_fwd_bwd(ea, t, w, deterministic=False):
+    o, lse = ea.attn_fwd(t["q"], t["k"], t["v"], causal=w.causal, softmax_scale=w.scale)
+    dq, dk, dv = ea.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=w.causal, softmax_scale=w.scale,
+                             deterministic=deterministic)
+    torch.cuda.synchronize()
+    ea.attn_get_device_status()
+    return dq, dk, dv
+
+
+def check_pairs(t, w, dq, dk, dv, pairs):
+    q, k, v, do = (t[n].cpu() for n in ("q", "k", "v", "do"))
+    out = []
+    for b, h in pairs:
+        ref = attention_bwd(q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h], w.scale, w.causal, row_block=2048)
+        out.append(check_grads({"dq": dq[b, :, h], "dk": dk[b, :, h], "dv": dv[b, :, h]}, ref,
+                               f"{w.name} b{b} h{h}"))
+    return out
+
+
+def test_single_head_d64(ea):
+    w = workloads.single_head_d64()
+    t = workloads.make_dense(w, device="cuda")
+    dq, dk, dv = gpu_fwd_bwd(ea, t, w)
+    check_pairs(t, w, dq, dk, dv, [(0, 0)])
+
+
+@pytest.mark.parametrize("dims", DIMS)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("nq,nk", [(1, 1), (17, 17), (128, 128), (200, 200), (257, 257), (513, 513),
+                                   (100, 300), (300, 100), (384, 640)])
+def test_small_shapes_full(ea, dims, causal, nq, nk):
+    dqk, dv_ = dims
+    w = workloads.Workload("small", 2, 3, nq, nk, dqk, dv_, causal, seed=nq * 7 + nk)
+    t = workloads.make_dense(w, device="cuda")
+    dq, dk, dv = gpu_fwd_bwd(ea, t, w)
+    check_pairs(t, w, dq, dk, dv, [(b, h) for b in range(2) for h in range(3)])
+
+
+def test_bwd_training_shape_sampled_and_deterministic(ea):
+    w = workloads.bwd_d128_N16384()
+    t = workloads.make_dense(w, device="cuda")
+    o, lse = ea.attn_fwd(t["q"], t["k"], t["v"], causal=True, softmax_scale=w.scale)
+    grads = None
+    for det in (True, False):
+        first = None
+        for rep in range(10 if det else 2):
+            g = ea.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=True, softmax_scale=w.scale,
+                            deterministic=det)
+            if first is None:
+                first = [x.clone() for x in g]
+            else:
+                for a, b in zip(first, g):
+                    assert torch.equal(a, b), "backward is not bitwise reproducible"
+        grads = first
+    ea.attn_get_device_status()
+    check_pairs(t, w, *grads, workloads.sample_pairs(w.batch, w.heads, 2, seed=16384))
+
+
+def test_mla_192_128_sampled(ea):
+    w = workloads.mla_192_128()
+    t = workloads.make_dense(w, device="cuda")
+    dq, dk, dv = gpu_fwd_bwd(ea, t, w)
+    check_pairs(t, w, dq, dk, dv, workloads.sample_pairs(w.batch, w.heads, 2, seed=192))
+
+
+def test_varlen_sampled(ea):
+    w = workloads.varlen_32seq()
+    t = workloads.make_varlen(w, device="cuda")
+    cu = t["cu_seqlens"]
+    L = max(w.varlen_lengths)
+    o, lse = ea.attn_fwd_varlen(t["q"], t["k"], t["v"], cu, cu, L, L, causal=True, softmax_scale=w.scale)
+    dq, dk, dv = ea.attn_bwd_varlen(t["q"], t["k"], t["v"], o, lse, t["do"], cu, cu, L, L, causal=True,
+                                    softmax_scale=w.scale)
+    torch.cuda.synchronize()
+    ea.attn_get_device_status()
+    lens = list(w.varlen_lengths)
+    cu_h = cu.cpu().numpy()
+    q, k, v, do = (t[n].cpu() for n in ("q", "k", "v", "do"))
+    for s, h in [(lens.index(max(lens)), 5), (lens.index(min(lens)), 30), (3, 0)]:
+        a, b = int(cu_h[s]), int(cu_h[s + 1])
+        ref = attention_bwd(q[a:b, h], k[a:b, h], v[a:b, h], do[a:b, h], w.scale, True, row_block=2048)
+        check_grads({"dq": dq[a:b, h], "dk": dk[a:b, h], "dv": dv[a:b, h]}, ref, f"varlen seq{s} h{h}")
+
+
+@pytest.mark.parametrize("dims", DIMS)
+def test_varlen_small_full(ea, dims):
+    dqk, dv_ = dims
+    lens = [1, 130, 0, 257, 64, 300]
+    w = workloads.Workload("vl", 1, 2, max(lens), max(lens), dqk, dv_, True, seed=9, varlen_lengths=tuple(lens))
+    t = workloads.make_varlen(w, device="cuda")
+    cu = t["cu_seqlens"]
+    L = max(lens)
+    o, lse = ea.attn_fwd_varlen(t["q"], t["k"], t["v"], cu, cu, L, L, causal=True, softmax_scale=w.scale)
+    dq, dk, dv = ea.attn_bwd_varlen(t["q"], t["k"], t["v"], o, lse, t["do"], cu, cu, L, L, causal=True,
+                                    softmax_scale=w.scale)
+    torch.cuda.synchronize()
+    cu_h = cu.cpu().numpy()
+    q, k, v, do = (t[n].cpu() for n in ("q", "k", "v", "do"))
+    for s in range(len(lens)):
+        a, b = int(cu_h[s]), int(cu_h[s + 1])
+        if b == a:
+            continue
+        for h in range(2):
+            ref = attention_bwd(q[a:b, h], k[a:b, h], v[a:b, h], do[a:b, h], w.scale, True)
+            check_grads({"dq": dq[a:b, h], "dk": dk[a:b, h], "dv": dv[a:b, h]}, ref, f"vl seq{s} h{h}")
+
+
+def test_autograd_wrapper_and_strided_views(ea):
+    g = torch.Generator(device="cuda").manual_seed(3)
+    qkv = torch.randn((2, 260, 3, 4, 128), generator=g, device="cuda").to(torch.bfloat16).requires_grad_(True)
+    q, k, v = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
+    do = torch.randn((2, 260, 4, 128), generator=g, device="cuda").to(torch.bfloat16)
+    o = ea.attention(q, k, v, causal=True)
+    o.backward(do)
+    grad = qkv.grad
+    qc, kc, vc, doc = (x.detach().cpu() for x in (q, k, v, do))
+    for b in range(2):
+        for h in range(4):
+            ref = attention_bwd(qc[b, :, h], kc[b, :, h], vc[b, :, h], doc[b, :, h], 128 ** -0.5, True)
+            check_grads({"dq": grad[b, :, 0, h], "dk": grad[b, :, 1, h], "dv": grad[b, :, 2, h]}, ref, "autograd")
+
+
+def test_degenerate_shapes(ea):
+    q = torch.randn((1, 5, 2, 64), device="cuda").to(torch.bfloat16)
+    kv0 = torch.empty((1, 0, 2, 64), device="cuda", dtype=torch.bfloat16)
+    o, lse = ea.attn_fwd(q, kv0, kv0)
+    dq, dk, dv = ea.attn_bwd(q, kv0, kv0, o, lse, torch.ones_like(q))
+    torch.cuda.synchronize()
+    assert torch.all(dq == 0)
+
+
+def test_workspace_errors(ea):
+    import ctypes
+    from exact_attention_bf16_gb300 import _abi
+    w = workloads.single_head_d64()
+    t = workloads.make_dense(w, device="cuda")
+    o, lse = ea.attn_fwd(t["q"], t["k"], t["v"], softmax_scale=w.scale)
+    p = _abi.AttnBwdParams()
+    ea._fill_fwd(p.fwd, t["q"], t["k"], t["v"], o, lse, ea._strides4, w.scale, False)
+    p.fwd.batch, p.fwd.seqlen_q, p.fwd.seqlen_k = 1, 128, 128
+    dq, dk, dv = (torch.empty_like(t[n]) for n in ("q", "k", "v"))
+    ea._fill_bwd(p, t["do"], dq, dk, dv, ea._strides4, False)
+    lib = _abi.load()
+    need = lib.attn_bwd_workspace_size(ctypes.byref(p))
+    assert need >= 128 * 4
+    assert lib.attn_bwd(ctypes.byref(p), None, 0, None) == _abi.ATTN_ERR_WORKSPACE
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    assert lib.attn_bwd(ctypes.byref(p), ctypes.c_void_p(ws.data_ptr()), need - 16, None) == _abi.ATTN_ERR_WORKSPACE
+    assert lib.attn_bwd(ctypes.byref(p), ctypes.c_void_p(ws.data_ptr()), need, None) == _abi.ATTN_OK
+    torch.cuda.synchronize()
