@@ -154,9 +154,24 @@ def _fill_bwd(p: AttnBwdParams, do, dq, dk, dv, strides, deterministic):
     p.deterministic = 1 if deterministic else 0
 
 
+def _event_handles(events):
+    if events is None:
+        return None
+    out = []
+    for ev in events:
+        if ev is None:
+            out.append(None)
+            continue
+        if getattr(ev, "cuda_event", 0) == 0:  # torch creates the CUDA event lazily
+            ev.record()
+        out.append(ev.cuda_event)
+    return out
+
+
 def attn_bwd(q, k, v, out, lse, dout, *, causal: bool = False, softmax_scale: Optional[float] = None,
-             deterministic: bool = False, dq=None, dk=None, dv=None, stream=None):
-    """Dense backward: returns (dQ, dK, dV) bf16 for the loss <O, dO>."""
+             deterministic: bool = False, dq=None, dk=None, dv=None, stream=None, phase_events=None):
+    """Dense backward: returns (dQ, dK, dV) bf16 for the loss <O, dO>. ``phase_events`` (optional, three
+    torch.cuda.Event) are recorded after the D pass, the dK/dV kernel and the dQ kernel."""
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
         _check_bf16(n, t, 4)
     B, Nq, H, dqk = q.shape
@@ -169,6 +184,10 @@ def attn_bwd(q, k, v, out, lse, dout, *, causal: bool = False, softmax_scale: Op
     _fill_fwd(p.fwd, q, k, v, out, lse, _strides4, scale, causal)
     p.fwd.batch, p.fwd.seqlen_q, p.fwd.seqlen_k = B, Nq, Nk
     _fill_bwd(p, dout, dq, dk, dv, _strides4, deterministic)
+    handles = _event_handles(phase_events)
+    if handles is not None:
+        for i, h in enumerate(handles):
+            p.phase_events[i] = h
     ws, nbytes = _workspace(_lib.attn_bwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_bwd(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_bwd")
     return dq, dk, dv

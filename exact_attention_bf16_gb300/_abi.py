@@ -51,6 +51,7 @@ class AttnBwdParams(ctypes.Structure):
         ("dk_batch_stride", c_i64), ("dk_row_stride", c_i64), ("dk_head_stride", c_i64),
         ("dv_batch_stride", c_i64), ("dv_row_stride", c_i64), ("dv_head_stride", c_i64),
         ("deterministic", c_i32), ("reserved0", c_i32),
+        ("phase_events", c_vp * 3),
     ]
 
 

@@ -91,6 +91,21 @@ attn_status_t make_map(CUtensorMap* m, const void* base, int d, int n_heads, int
   return ATTN_OK;
 }
 
+// Makes the device that owns `ptr` current for this library's runtime on the
+// calling thread (entry points may be called from threads, such as an
+// autograd worker, on which this library has not yet touched the device).
+cudaError_t bind_device_of(const void* ptr) {
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
+  if (e != cudaSuccess) return e;
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return cudaErrorInvalidDevicePointer;
+  int cur = -1;
+  e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return e;
+  if (cur != attr.device) return cudaSetDevice(attr.device);
+  return cudaFree(nullptr);  // ensures the primary context is current on this thread
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool stride_ok(int64_t s) { return s >= 0 && (s % 8) == 0 && s < (int64_t(1) << 38); }
 
@@ -119,8 +134,9 @@ attn_status_t check_common(const attn_fwd_params* p, bool varlen) {
   return ATTN_OK;
 }
 
-attn_status_t check_tensor(const void* ptr, int64_t sb, int64_t sn, int64_t sh, bool varlen) {
-  if (!ptr || !aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
+// A tensor with no rows may have a null base pointer (an empty allocation).
+attn_status_t check_tensor(const void* ptr, int64_t sb, int64_t sn, int64_t sh, bool varlen, bool empty = false) {
+  if ((!ptr && !empty) || !aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
   if (!stride_ok(sn) || !stride_ok(sh)) return ATTN_ERR_INVALID_ARG;
   if (!varlen && !stride_ok(sb)) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
@@ -132,13 +148,17 @@ attn_status_t check_tensor(const void* ptr, int64_t sb, int64_t sn, int64_t sh, 
     if (_s != ATTN_OK) return _s;          \
   } while (0)
 
+bool no_q_rows(const attn_fwd_params* p, bool varlen) { return (varlen ? p->total_q : p->seqlen_q) == 0; }
+bool no_k_rows(const attn_fwd_params* p, bool varlen) { return (varlen ? p->total_k : p->seqlen_k) == 0; }
+
 attn_status_t check_fwd(const attn_fwd_params* p, bool varlen) {
   ATTN_TRY(check_common(p, varlen));
-  ATTN_TRY(check_tensor(p->q, p->q_batch_stride, p->q_row_stride, p->q_head_stride, varlen));
-  ATTN_TRY(check_tensor(p->k, p->k_batch_stride, p->k_row_stride, p->k_head_stride, varlen));
-  ATTN_TRY(check_tensor(p->v, p->v_batch_stride, p->v_row_stride, p->v_head_stride, varlen));
-  ATTN_TRY(check_tensor(p->o, p->o_batch_stride, p->o_row_stride, p->o_head_stride, varlen));
-  if (!p->lse || (reinterpret_cast<uintptr_t>(p->lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  const bool eq = no_q_rows(p, varlen), ek = no_k_rows(p, varlen);
+  ATTN_TRY(check_tensor(p->q, p->q_batch_stride, p->q_row_stride, p->q_head_stride, varlen, eq));
+  ATTN_TRY(check_tensor(p->k, p->k_batch_stride, p->k_row_stride, p->k_head_stride, varlen, ek));
+  ATTN_TRY(check_tensor(p->v, p->v_batch_stride, p->v_row_stride, p->v_head_stride, varlen, ek));
+  ATTN_TRY(check_tensor(p->o, p->o_batch_stride, p->o_row_stride, p->o_head_stride, varlen, eq));
+  if ((!p->lse && !eq) || (reinterpret_cast<uintptr_t>(p->lse) & 3u)) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
@@ -149,6 +169,10 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
   const int units = varlen ? p->num_seqs : p->batch;
   const int max_q = varlen ? p->max_seqlen_q : p->seqlen_q;
   if (nq_rows == 0 || max_q == 0) return ATTN_OK;
+  {
+    cudaError_t be = bind_device_of(p->q ? p->q : p->k);
+    if (be != cudaSuccess) return be == cudaErrorInvalidDevicePointer ? ATTN_ERR_INVALID_ARG : cuda_fail(be, "device");
+  }
 
   FwdArgs a{};
   a.o = p->o;
@@ -210,12 +234,18 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
   if (!p) return ATTN_ERR_INVALID_ARG;
   const attn_fwd_params& f = p->fwd;
   ATTN_TRY(check_fwd(&f, varlen));
-  ATTN_TRY(check_tensor(p->dout, p->do_batch_stride, p->do_row_stride, p->do_head_stride, varlen));
-  ATTN_TRY(check_tensor(p->dq, p->dq_batch_stride, p->dq_row_stride, p->dq_head_stride, varlen));
-  ATTN_TRY(check_tensor(p->dk, p->dk_batch_stride, p->dk_row_stride, p->dk_head_stride, varlen));
-  ATTN_TRY(check_tensor(p->dv, p->dv_batch_stride, p->dv_row_stride, p->dv_head_stride, varlen));
+  const bool eq = no_q_rows(&f, varlen), ek = no_k_rows(&f, varlen);
+  ATTN_TRY(check_tensor(p->dout, p->do_batch_stride, p->do_row_stride, p->do_head_stride, varlen, eq));
+  ATTN_TRY(check_tensor(p->dq, p->dq_batch_stride, p->dq_row_stride, p->dq_head_stride, varlen, eq));
+  ATTN_TRY(check_tensor(p->dk, p->dk_batch_stride, p->dk_row_stride, p->dk_head_stride, varlen, ek));
+  ATTN_TRY(check_tensor(p->dv, p->dv_batch_stride, p->dv_row_stride, p->dv_head_stride, varlen, ek));
   const int nq_rows = varlen ? f.total_q : f.seqlen_q;
   const int nk_rows = varlen ? f.total_k : f.seqlen_k;
+  if (nq_rows == 0 && nk_rows == 0) return ATTN_OK;
+  {
+    cudaError_t be = bind_device_of(nq_rows ? f.q : f.k);
+    if (be != cudaSuccess) return be == cudaErrorInvalidDevicePointer ? ATTN_ERR_INVALID_ARG : cuda_fail(be, "device");
+  }
   const size_t need = bwd_workspace_bytes(p, varlen);
   if (nq_rows > 0 && nk_rows > 0 && (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u)))
     return ATTN_ERR_WORKSPACE;
@@ -271,11 +301,17 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
                     qrows));
   ATTN_TRY(make_map(&tdo2, p->dout, f.d_v, f.heads, nq_rows, nb, p->do_batch_stride, p->do_row_stride,
                     p->do_head_stride, qrows));
+  auto mark = [&](int i) -> cudaError_t {
+    return p->phase_events[i] ? cudaEventRecord(static_cast<cudaEvent_t>(p->phase_events[i]), stream) : cudaSuccess;
+  };
   e = launch_bwd_preprocess(f.d_v, a, stream);
+  if (e == cudaSuccess) e = mark(0);
   if (e != cudaSuccess) return cuda_fail(e, "bwd preprocess launch");
   e = launch_bwd_dkdv(f.d_qk, f.d_v, tq2, tk, tv, tdo2, a, stream);
+  if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return cuda_fail(e, "bwd dkdv launch");
   e = launch_bwd_dq(f.d_qk, f.d_v, tq, tk, tv, tdo, a, stream);
+  if (e == cudaSuccess) e = mark(2);
   if (e != cudaSuccess) return cuda_fail(e, "bwd dq launch");
   return ATTN_OK;
 }
@@ -321,6 +357,11 @@ attn_status_t attn_bwd_varlen(const attn_bwd_params* p, void* workspace, size_t 
 
 attn_status_t attn_exp2_eval(const float* x, float* y_poly, float* y_hw, int64_t n, attn_stream_t stream) {
   if (n < 0 || (n > 0 && !x) || (!y_poly && !y_hw)) return ATTN_ERR_INVALID_ARG;
+  if (n == 0) return ATTN_OK;
+  {
+    cudaError_t be = bind_device_of(x);
+    if (be != cudaSuccess) return be == cudaErrorInvalidDevicePointer ? ATTN_ERR_INVALID_ARG : cuda_fail(be, "device");
+  }
   cudaError_t e = launch_exp2_eval(x, y_poly, y_hw, n, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "exp2 eval launch");
 }

@@ -162,12 +162,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sDv = sLSE + QB;                                      // [QB]
   DkdvBars* bar = reinterpret_cast<DkdvBars*>(smem + C::OFF_BAR);
 
-  // heaviest key tiles first under the causal mask (tile 0 sees every query)
-  const int per = a.num_units * a.heads;
-  const int n = static_cast<int>(blockIdx.x) / per;
-  const int rem = static_cast<int>(blockIdx.x) % per;
-  const int h = rem % a.heads;
-  const Unit U = unit_bounds(a, rem / a.heads);
+  // (unit, head) is the slow index so that resident CTAs share a few heads'
+  // Q/dO in L2; within a head the heaviest key tiles (tile 0 sees every query
+  // under the causal mask) come first.
+  const int bh = static_cast<int>(blockIdx.x) / a.n_kblk;
+  const int n = static_cast<int>(blockIdx.x) % a.n_kblk;
+  const int h = bh % a.heads;
+  const Unit U = unit_bounds(a, bh / a.heads);
   const int k0 = n * KB;
   if (k0 >= U.nk) return;
   int m_begin = 0;
@@ -444,11 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sDS = smem + C::OFF_DS;
   DqBars* bar = reinterpret_cast<DqBars*>(smem + C::OFF_BAR);
 
-  const int per = a.num_units * a.heads;
-  const int m = a.n_qblk - 1 - static_cast<int>(blockIdx.x) / per;  // heaviest (last) query tiles first
-  const int rem = static_cast<int>(blockIdx.x) % per;
-  const int h = rem % a.heads;
-  const Unit U = unit_bounds(a, rem / a.heads);
+  // (unit, head) slow for L2 sharing of K/V; heaviest (last) query tiles first within a head
+  const int bh = static_cast<int>(blockIdx.x) / a.n_qblk;
+  const int m = a.n_qblk - 1 - static_cast<int>(blockIdx.x) % a.n_qblk;
+  const int h = bh % a.heads;
+  const Unit U = unit_bounds(a, bh / a.heads);
   const int q0 = m * MB;
   if (q0 >= U.nq) return;
   const int last = min(q0 + MB - 1, U.nq - 1);

@@ -16,7 +16,10 @@
 // running max m_used is replaced only when a new tile's row max exceeds it by
 // more than 8.0, in which case O and l are multiplied by 2^(m_old - m_new);
 // otherwise the stale max is kept (p <= 2^8). The epilogue divides by the
-// exact row sum l, which makes the result independent of the skipped rescales.
+// exact row sum, which makes the result independent of the skipped rescales.
+// Two row sums are kept: O is divided by the sum of the bf16-rounded p that the
+// P V product consumes (so the weights applied to V sum to one exactly), LSE
+// uses the sum of the unrounded fp32 p.
 // exp2 runs on the hardware unit for most columns and on the FMA pipe
 // (exp2_emu.cuh) for a fixed 1/EMU_PERIOD of them (same page, section
 // 用软件"伪造"硬件指令).
@@ -36,6 +39,7 @@ constexpr int kThreads = 384;   // 12 warps
 constexpr int kChunk = BM * 128;  // bytes of one 64-column (128-byte) swizzled chunk of a 128-row tile
 constexpr float kThreshold = 8.0f;  // log2 units (factor 256)
 
+
 // TMEM column map (512 columns allocated): S/P for tile i at tS(i), O at tO(i).
 __host__ __device__ constexpr uint32_t tS(int i) { return 128u * i; }
 __host__ __device__ constexpr uint32_t tO(int i) { return 256u + 128u * i; }
@@ -52,6 +56,12 @@ struct Cfg {
   static constexpr int BAR_OFF = QT * Q_BYTES + NSLOT * SLOT;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;  // barriers + alignment slack
   static_assert(SMEM <= 232448, "shared memory budget");
+  // Register split: warpgroup 0 (TMA, MMA, two idle warps) gives registers to
+  // the two softmax warpgroups. 128*REG_LO + 256*REG_HI must fit in the
+  // 384 * (launch registers per thread) the CTA starts with (checked on the host).
+  static constexpr uint32_t REG_LO = DQK == 192 ? 72 : 56;
+  static constexpr uint32_t REG_HI = DQK == 192 ? 192 : 200;
+  static constexpr int REG_BUDGET = 128 * REG_LO + 256 * REG_HI;
 };
 
 struct Bars {
@@ -85,12 +95,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sKV = smem + QT * C::Q_BYTES;
   Bars* bar = reinterpret_cast<Bars*>(smem + C::BAR_OFF);
 
-  // ---- work unit: heaviest 256-row blocks first (causal) --------------------
-  const int per_blk = a.num_units * a.heads;
-  const int mblk = a.n_mblk - 1 - static_cast<int>(blockIdx.x) / per_blk;
-  const int rem = static_cast<int>(blockIdx.x) % per_blk;
-  const int unit = rem / a.heads;
-  const int h = rem % a.heads;
+  // ---- work unit ------------------------------------------------------------
+  // (unit, head) is the slow index so that the CTAs resident at any time share
+  // a few heads' K/V in L2 (all heads' K/V together exceed it); within a head
+  // the heaviest (last, under the causal mask) 256-row blocks come first.
+  const int bh = static_cast<int>(blockIdx.x) / a.n_mblk;
+  const int mblk = a.n_mblk - 1 - static_cast<int>(blockIdx.x) % a.n_mblk;
+  const int unit = bh / a.heads;
+  const int h = bh % a.heads;
   int q_start = 0, k_start = 0, nq = a.seqlen_q, nk = a.seqlen_k, b = unit;
   if (a.cu_q != nullptr) {
     q_start = a.cu_q[unit];
@@ -139,6 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = bar->tmem_base;
 
+  if (warp < 4) {
+  regs_dec<C::REG_LO>();
   if (warp == 0) {
     // ======================= TMA producer ===================================
     if (lane == 0) {
@@ -233,7 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bar->mma_done);
       mbar_wait(&bar->mma_done, 0, a.status, 0x2ff);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+    regs_inc<C::REG_HI>();
     // ======================= softmax + correction ===========================
     const int i = (warp - 4) / 4;          // query tile
     const uint32_t quarter = warp & 3u;    // TMEM lane quarter this warp may access
@@ -243,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tbase + ((quarter * 32u) << 16);
     const float sl2 = a.scale_log2;
     float m_used = -INFINITY;  // log2 units
-    float l = 0.f;
+    float l = 0.f;   // row sum of the bf16-rounded weights (divides O)
+    float lx = 0.f;  // row sum of the fp32 weights (LSE)
     int n_rescale = 0, n_opp = 0;
     bool ok = true;
     for (int j = 0; j < nkv[i]; ++j) {
@@ -262,9 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN; ++c)
           if (c >= cnt) s[c] = __float_as_uint(-INFINITY);
       }
-      float mx = __uint_as_float(s[0]);
+      // row max as 8 independent chains, then a tree (no 128-long dependency chain)
+      float mp[8];
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+      for (int c = 0; c < 8; ++c) mp[c] = __uint_as_float(s[c]);
+#pragma unroll
+      for (int c = 8; c < BN; ++c) mp[c % 8] = fmaxf(mp[c % 8], __uint_as_float(s[c]));
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       const float m_tile = mx * sl2;
       const bool need = m_tile > m_used + kThreshold;
       float alpha = 1.f;
@@ -277,26 +298,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         n_rescale += need;
       }
       l *= alpha;
+      lx *= alpha;
       const float mu = (m_used == -INFINITY) ? 0.f : m_used;
       // p = 2^(s * scale * log2e - m_used), packed to bf16 pairs in place
       uint32_t pk[BN / 2];
-      float rs = 0.f;
+      float2 rsp[2], rsx[2];  // partial sums: bf16-rounded p (normalises O), fp32 p (gives LSE)
+#pragma unroll
+      for (int z = 0; z < 2; ++z) rsp[z] = rsx[z] = make_float2(0.f, 0.f);
+      const float2 sl2v = make_float2(sl2, sl2), negmu = make_float2(-mu, -mu);
 #pragma unroll
       for (int c = 0; c < BN / 2; ++c) {
-        const float x0 = fmaf(__uint_as_float(s[2 * c]), sl2, -mu);
-        const float x1 = fmaf(__uint_as_float(s[2 * c + 1]), sl2, -mu);
+        const float2 x = ffma2(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sl2v, negmu);
         float p0, p1;
         if (EMU_PERIOD > 0 && ((2 * c) % EMU_PERIOD) == EMU_PERIOD - 2) {
-          p0 = ex2_mufu(x0);
-          p1 = ex2_emu(x1);
+          p0 = ex2_mufu(x.x);
+          p1 = ex2_emu(x.y);
         } else {
-          p0 = ex2_mufu(x0);
-          p1 = ex2_mufu(x1);
+          p0 = ex2_mufu(x.x);
+          p1 = ex2_mufu(x.y);
         }
-        rs += p0 + p1;
         pk[c] = pack_bf16x2(p0, p1);
+        rsp[c % 2].x += __uint_as_float(pk[c] << 16);
+        rsp[c % 2].y += __uint_as_float(pk[c] & 0xffff0000u);
+        rsx[c % 2].x += p0;
+        rsx[c % 2].y += p1;
       }
-      l += rs;
+      l += (rsp[0].x + rsp[0].y) + (rsp[1].x + rsp[1].y);
+      lx += (rsx[0].x + rsx[0].y) + (rsx[1].x + rsx[1].y);
       tmem_st32(lane_base + tS(i) + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st32(lane_base + tS(i) + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       // correction: rescale this tile's O rows whose max moved (warp-uniform branch)
@@ -352,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (store) {
-      const float lse = (l > 0.f) ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      const float lse = (lx > 0.f) ? (m_used + log2f(lx)) * 0.69314718055994531f : -INFINITY;
       a.lse[static_cast<int64_t>(b) * a.lse_sb + static_cast<int64_t>(h) * a.lse_sh + q_start + row] = lse;
     }
   }
@@ -395,10 +423,15 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
                      cudaStream_t stream) {
   using C = Cfg<DQK, DV>;
   auto kern = attn_fwd_kernel<DQK, DV, kEmuPeriod>;
-  static bool attr_done = false;  // benign race: the attribute call is idempotent
+  static bool attr_done = false;  // benign race: the attribute calls are idempotent
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    // The setmaxnreg split must fit in the registers the CTA is launched with.
+    if (fa.numRegs * kThreads < C::REG_BUDGET) return cudaErrorInvalidConfiguration;
     attr_done = true;
   }
   const int64_t grid = static_cast<int64_t>(a.n_mblk) * a.num_units * a.heads;

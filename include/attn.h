@@ -128,6 +128,10 @@ typedef struct attn_bwd_params {
   int64_t dv_batch_stride, dv_row_stride, dv_head_stride;
   int32_t deterministic;
   int32_t reserved0;
+  /* Optional (each may be NULL): CUDA events (cudaEvent_t) recorded on the
+   * stream after the D = rowsum(dO * O) pass [0], after the dK/dV kernel [1]
+   * and after the dQ kernel [2], for timing the phases. */
+  void* phase_events[3];
 } attn_bwd_params;
 
 /* Bytes of device workspace the matching call needs (0 means none: pass NULL). */
