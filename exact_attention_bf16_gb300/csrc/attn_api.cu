@@ -99,11 +99,8 @@ cudaError_t bind_device_of(const void* ptr) {
   cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
   if (e != cudaSuccess) return e;
   if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return cudaErrorInvalidDevicePointer;
-  int cur = -1;
-  e = cudaGetDevice(&cur);
-  if (e != cudaSuccess) return e;
-  if (cur != attr.device) return cudaSetDevice(attr.device);
-  return cudaFree(nullptr);  // ensures the primary context is current on this thread
+  // cudaSetDevice also makes the device's primary context current on this thread.
+  return cudaSetDevice(attr.device);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
