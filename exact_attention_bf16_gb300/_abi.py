@@ -11,6 +11,7 @@ LIB_PATH = os.path.join(HERE, "libattn_gb300.so")
 HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "attn.h")
 
 ABI_VERSION = 1
+BWD_NOALLOC_SCRATCH_BYTES = 8 << 20  # ATTN_BWD_NOALLOC_SCRATCH_BYTES
 
 STATUS = {
     0: "ATTN_OK",
@@ -76,6 +77,7 @@ def load(path: str = LIB_PATH):
         "attn_fwd_varlen": (ctypes.c_int, [P(AttnFwdParams), c_vp, ctypes.c_size_t, c_vp]),
         "attn_bwd": (ctypes.c_int, [P(AttnBwdParams), c_vp, ctypes.c_size_t, c_vp]),
         "attn_bwd_varlen": (ctypes.c_int, [P(AttnBwdParams), c_vp, ctypes.c_size_t, c_vp]),
+        "attn_bwd_noalloc": (ctypes.c_int, [P(AttnBwdParams), c_vp]),
         "attn_exp2_eval": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i64, c_vp]),
         "attn_get_device_status": (ctypes.c_int, [c_vp, P(ctypes.c_uint32)]),
         "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),

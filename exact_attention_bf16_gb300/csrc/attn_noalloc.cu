@@ -1,0 +1,74 @@
+// attn_bwd_noalloc: the backward pass for callers that cannot allocate device
+// memory. It needs no counterpart in the attention method itself; it only
+// changes where the backward's scratch lives.
+//
+// Who needs it: code that runs where allocation is not allowed or not
+// possible, for example an inference or training runtime that plans all
+// device memory up front and forbids cudaMalloc afterwards (a fixed memory
+// budget, or a pool that owns the whole device), a plugin whose host
+// framework hands it only the tensors, or a latency-sensitive loop in which a
+// cudaMalloc (which may synchronise the device) is not acceptable. attn_bwd
+// asks such callers for a workspace they would have to allocate; this entry
+// point takes none.
+//
+// The scratch (D_i = dO_i . O_i, 4 bytes per (batch, head, query row)) lives
+// in a file-scope __device__ array of ATTN_BWD_NOALLOC_SCRATCH_BYTES, which
+// every GPU that loads this library holds until the process exits. On the
+// first call on a device the array's device address is looked up with
+// cudaGetSymbolAddress (with that device current) and cached; that first call
+// should therefore come before any stream capture. Larger problems are
+// rejected with ATTN_ERR_WORKSPACE. All calls share the one array: calls that
+// can overlap on the GPU (different streams, or another thread) race on it and
+// must be serialised by the caller. Nothing in the array has to start at zero:
+// the D pass writes every entry that the dK/dV and dQ kernels read, so the
+// previous call's contents are never used.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/attn.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_bwd_scratch[ATTN_BWD_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+// Device address of g_bwd_scratch on `dev`, which must be the current device.
+cudaError_t scratch_address(int dev, void** out) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_bwd_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = ptr;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" attn_status_t attn_bwd_noalloc(const attn_bwd_params* p, attn_stream_t stream) {
+  if (!p) return ATTN_ERR_INVALID_ARG;
+  const bool varlen = p->fwd.cu_seqlens_q != nullptr;
+  const size_t need = attn_bwd_workspace_size(p);
+  if (need > ATTN_BWD_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;  // problem too large for the fixed scratch
+  const int nq = varlen ? p->fwd.total_q : p->fwd.seqlen_q;
+  const int nk = varlen ? p->fwd.total_k : p->fwd.seqlen_k;
+  void* ws = nullptr;
+  if (nq > 0 && nk > 0) {
+    // Set-up: make the data's device current, then resolve the array's address on it.
+    cudaPointerAttributes attr{};
+    if (!p->fwd.q || cudaPointerGetAttributes(&attr, p->fwd.q) != cudaSuccess ||
+        (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged))
+      return ATTN_ERR_INVALID_ARG;
+    if (cudaSetDevice(attr.device) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (scratch_address(attr.device, &ws) != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return varlen ? attn_bwd_varlen(p, ws, ATTN_BWD_NOALLOC_SCRATCH_BYTES, stream)
+                : attn_bwd(p, ws, ATTN_BWD_NOALLOC_SCRATCH_BYTES, stream);
+}

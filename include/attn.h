@@ -149,6 +149,24 @@ attn_status_t attn_bwd(const attn_bwd_params* p, void* workspace, size_t workspa
 attn_status_t attn_bwd_varlen(const attn_bwd_params* p, void* workspace, size_t workspace_bytes,
                               attn_stream_t stream);
 
+/* Backward for callers that cannot allocate device memory (an engine that
+ * plans all memory up front and forbids later cudaMalloc, a plugin that is
+ * handed only tensors, a loop where an allocation's possible device
+ * synchronisation is unacceptable). Same computation and arguments as
+ * attn_bwd / attn_bwd_varlen (chosen by whether fwd.cu_seqlens_q is NULL), but
+ * no workspace: the scratch lives in a fixed array inside the library of
+ * ATTN_BWD_NOALLOC_SCRATCH_BYTES bytes per GPU that loads the library, held
+ * until process exit. The attention method has no counterpart to this entry
+ * point; it exists only for these callers. Limit: attn_bwd_workspace_size(p)
+ * must not exceed ATTN_BWD_NOALLOC_SCRATCH_BYTES (4 bytes per batch x head x
+ * query row, so up to 2,097,152 such rows), else ATTN_ERR_WORKSPACE and
+ * nothing is launched. The first call on each device resolves the array's
+ * address and should come before any stream capture. All calls share the one
+ * array: calls that may overlap on the GPU race and must be serialised by the
+ * caller. Allocates nothing (no cudaMalloc, no cudaFree). */
+#define ATTN_BWD_NOALLOC_SCRATCH_BYTES (8u << 20)
+attn_status_t attn_bwd_noalloc(const attn_bwd_params* p, attn_stream_t stream);
+
 /* Diagnostic: evaluates the kernels' two exp2 paths on n device floats x:
  * y_poly = Cody-Waite split + cubic on the FMA pipe (NULL to skip),
  * y_hw = the hardware ex2 approximation (NULL to skip). Same code as the
