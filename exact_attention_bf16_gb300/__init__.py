@@ -87,9 +87,10 @@ def _workspace(size: int, device) -> Tuple[Optional[torch.Tensor], int]:
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = False,
              softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
              lse: Optional[torch.Tensor] = None, rescale_stats: Optional[torch.Tensor] = None,
-             stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+             exp2_emu_period: int = 0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Dense forward. q [B, Nq, H, d_qk], k [B, Nk, H, d_qk], v [B, Nk, H, d_v] (bf16, CUDA).
-    Returns (O [B, Nq, H, d_v] bf16, LSE [B, H, Nq] fp32, natural log)."""
+    Returns (O [B, Nq, H, d_v] bf16, LSE [B, H, Nq] fp32, natural log). ``exp2_emu_period`` (0, 4, 8)
+    sends one column in that many of every row's exp2 to the FMA-pipe polynomial."""
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_bf16(n, t, 4)
     B, Nq, H, dqk = q.shape
@@ -108,6 +109,7 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool 
     _fill_fwd(p, q, k, v, out, lse, _strides4, scale, causal)
     p.batch, p.seqlen_q, p.seqlen_k = B, Nq, Nk
     p.rescale_stats = _ptr(rescale_stats)
+    p.exp2_emu_period = int(exp2_emu_period)
     ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_fwd(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_fwd")
     return out, lse
@@ -117,7 +119,7 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                     cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, *, causal: bool = False,
                     softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                     lse: Optional[torch.Tensor] = None, rescale_stats: Optional[torch.Tensor] = None,
-                    stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                    exp2_emu_period: int = 0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Packed variable-length forward. q [total_q, H, d_qk], k/v [total_k, H, d]; cu_seqlens int32 on
     the device. Returns (O [total_q, H, d_v], LSE [H, total_q])."""
     for n, t in (("q", q), ("k", k), ("v", v)):
@@ -140,6 +142,7 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
     p.total_q, p.total_k = tq, tk
     p.batch = 1
     p.rescale_stats = _ptr(rescale_stats)
+    p.exp2_emu_period = int(exp2_emu_period)
     ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_fwd_varlen(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_fwd_varlen")
     return out, lse

@@ -38,7 +38,7 @@ class AttnFwdParams(ctypes.Structure):
         ("cu_seqlens_q", c_vp), ("cu_seqlens_k", c_vp),
         ("num_seqs", c_i32), ("max_seqlen_q", c_i32), ("max_seqlen_k", c_i32),
         ("total_q", c_i32), ("total_k", c_i32),
-        ("softmax_scale", c_f32), ("causal", c_i32), ("reserved0", c_i32),
+        ("softmax_scale", c_f32), ("causal", c_i32), ("exp2_emu_period", c_i32),
         ("rescale_stats", c_vp),
     ]
 

@@ -161,6 +161,7 @@ attn_status_t check_fwd(const attn_fwd_params* p, bool varlen) {
 
 attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream) {
   ATTN_TRY(check_fwd(p, varlen));
+  if (p->exp2_emu_period != 0 && p->exp2_emu_period != 4 && p->exp2_emu_period != 8) return ATTN_ERR_INVALID_ARG;
   const int nq_rows = varlen ? p->total_q : p->seqlen_q;
   const int nk_rows = varlen ? p->total_k : p->seqlen_k;
   const int units = varlen ? p->num_seqs : p->batch;
@@ -190,6 +191,7 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
   a.scale_log2 = p->softmax_scale * 1.4426950408889634f;
   a.causal = p->causal ? 1 : 0;
   a.stats = p->rescale_stats;
+  a.emu_period = p->exp2_emu_period;
   cudaError_t e = status_ptr(&a.status);
   if (e != cudaSuccess) return cuda_fail(e, "status word");
 

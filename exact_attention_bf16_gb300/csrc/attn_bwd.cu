@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar->st_empty[s], 1);
     }
     mbar_init(&bar->s_full, 1);
-    mbar_init(&bar->ds_full, kSoftThreads);
+    mbar_init(&bar->ds_full, kSoftThreads / 32);  // one arrival per softmax warp
     mbar_init(&bar->acc_full, 1);
     mbar_init(&bar->mma_done, 1);
     fence_barrier_init();
@@ -304,10 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float l = a.lse[U.b * a.lse_sb + h * a.lse_sh + U.q_start + i];
             v = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
           }
-          sLSE[tid] = v;
+          sLSE[tid] = -v;  // stored negated: P = 2^(S * scale * log2e + sLSE)
         } else if (tid < 2 * QB) {
           const int i = q0 + tid - QB;
-          sDv[tid - QB] = (i < U.nq) ? a.dsum[U.b * a.lse_sb + h * a.lse_sh + U.q_start + i] : 0.f;
+          sDv[tid - QB] = (i < U.nq) ? -a.dsum[U.b * a.lse_sb + h * a.lse_sh + U.q_start + i] : 0.f;  // -D
         }
         named_bar_sync(1, kSoftThreads);
       }
@@ -322,18 +322,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(lane_base + C::tdP + col0, dp);
         tmem_wait_ld();
         uint32_t pw[16], dw[16];
+        const float2 sl2v = make_float2(sl2, sl2);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p[2], ds[2];
-#pragma unroll
-          for (int z = 0; z < 2; ++z) {
-            const int col = col0 + e + z;
-            const bool vis = key_ok && (q0 + col >= i_vis);
-            p[z] = vis ? ex2_mufu(fmaf(__uint_as_float(s[e + z]), sl2, -sLSE[col])) : 0.f;
-            ds[z] = p[z] * (__uint_as_float(dp[e + z]) - sDv[col]);
-          }
-          pw[e / 2] = pack_bf16x2(p[0], p[1]);
-          dw[e / 2] = pack_bf16x2(ds[0], ds[1]);
+          const int col = col0 + e;
+          // smem holds -LSE*log2e and -D per query column (broadcast reads)
+          const float2 nl = *reinterpret_cast<const float2*>(&sLSE[col]);
+          const float2 nd = *reinterpret_cast<const float2*>(&sDv[col]);
+          const float2 x = ffma2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sl2v, nl);
+          float2 p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+          if (!(key_ok && q0 + col >= i_vis)) p.x = 0.f;
+          if (!(key_ok && q0 + col + 1 >= i_vis)) p.y = 0.f;
+          const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
+          pw[e / 2] = pack_bf16x2(p.x, p.y);
+          dw[e / 2] = pack_bf16x2(ds.x, ds.y);
         }
         // P^T for these 32 queries goes to the first 16 columns of the S
         // columns this thread just read (never into columns the other
@@ -344,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar->ds_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar->ds_full);
     }
     // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
     if (ok && T > 0) {
@@ -420,6 +423,8 @@ struct DqBars {
   uint64_t st_full[2];
   uint64_t st_empty[2];
   uint64_t s_full;
+  uint64_t sp_free;   // softmax warps hold S(t), dP(t) in registers: TMEM may be overwritten
+  uint64_t ds_free;   // dQ(t) has read dS(t) from shared memory
   uint64_t ds_full;
   uint64_t acc_full;
   uint64_t mma_done;
@@ -463,7 +468,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar->st_empty[s], 1);
     }
     mbar_init(&bar->s_full, 1);
-    mbar_init(&bar->ds_full, kSoftThreads);
+    mbar_init(&bar->sp_free, kSoftThreads / 32);
+    mbar_init(&bar->ds_free, 1);
+    mbar_init(&bar->ds_full, kSoftThreads / 32);  // one arrival per softmax warp
     mbar_init(&bar->acc_full, 1);
     mbar_init(&bar->mma_done, 1);
     fence_barrier_init();
@@ -510,36 +517,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idQ = idesc_bf16_f32(MB, DQK, false, true);  // B = K tile, MN-major
       bool ok = mbar_wait(&bar->q_full, 0, a.status, 0x2200);
       const uint32_t qb = smem_u32(sQ), gb = smem_u32(sdO), dsb = smem_u32(sDS);
-      for (int t = 0; t < T && ok; ++t) {
+      // S(t) = Q K_t^T and dP(t) = dO V_t^T into TMEM, then signal the softmax warps.
+      auto issue_s_dp = [&](int t) -> bool {
         const int st = t % C::NST;
-        ok = mbar_wait(&bar->st_full[st], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x2210);
-        if (!ok) break;
+        if (!mbar_wait(&bar->st_full[st], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x2210)) return false;
         tc_fence_after();
         const uint32_t kb = smem_u32(sST + st * C::STAGE);
         const uint32_t vb = kb + C::K_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < DQK / 16; ++kk) {  // S = Q K^T
+        for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t off = (kk / 4) * MB * 128 + (kk % 4) * 32;
           mma_ss(tbase + C::tS, smem_desc(qb + off, 16, 1024, SWZ_128B), smem_desc(kb + off, 16, 1024, SWZ_128B), idS,
                  kk > 0 ? 1u : 0u);
         }
 #pragma unroll
-        for (int kk = 0; kk < DV / 16; ++kk) {  // dP = dO V^T
+        for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t off = (kk / 4) * MB * 128 + (kk % 4) * 32;
           mma_ss(tbase + C::tdP, smem_desc(gb + off, 16, 1024, SWZ_128B), smem_desc(vb + off, 16, 1024, SWZ_128B),
                  idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bar->s_full);
+        return true;
+      };
+      if (ok && T > 0) ok = issue_s_dp(0);
+      for (int t = 0; t < T && ok; ++t) {
+        const int st = t % C::NST;
+        // With two K/V stages the next tile's S and dP are computed while the
+        // softmax warps work on this one (they have already copied S(t), dP(t)).
+        if (C::NST > 1 && t + 1 < T) {
+          ok = mbar_wait(&bar->sp_free, static_cast<uint32_t>(t) & 1u, a.status, 0x2215);
+          if (ok) ok = issue_s_dp(t + 1);
+          if (!ok) break;
+        }
         ok = mbar_wait(&bar->ds_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2220);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t kb = smem_u32(sST + st * C::STAGE);
 #pragma unroll
         for (int kk = 0; kk < KB / 16; ++kk) {  // dQ += dS K   (B = K tile as [d][kv], MN-major)
           const uint64_t ad = smem_desc(dsb + (kk / 4) * MB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
           const uint64_t bd = smem_desc(kb + kk * 2048, KB * 128, 1024, SWZ_128B);
           mma_ss(tbase + C::tdQ, ad, bd, idQ, (t > 0 || kk > 0) ? 1u : 0u);
         }
+        mma_commit(&bar->ds_free);
         mma_commit(&bar->st_empty[st]);
+        if (C::NST == 1 && t + 1 < T) {
+          // one stage: the next K/V tile can only arrive after this dQ has read K(t)
+          ok = issue_s_dp(t + 1);
+          if (!ok) break;
+        }
       }
       mma_commit(&bar->acc_full);
       mma_commit(&bar->mma_done);
@@ -561,35 +587,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float sl2 = a.scale_log2;
     bool ok = true;
+    const float2 sl2v = make_float2(sl2, sl2), nl = make_float2(-lse2, -lse2), nd = make_float2(-dsum, -dsum);
     for (int t = 0; t < T; ++t) {
       ok = mbar_wait(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2300);
       if (!ok) break;
       tc_fence_after();
       const int cnt = lim - t * KB;  // visible keys of this row in tile t
+      // copy this warpgroup's 64 columns of S and dP out of TMEM, then release them
+      uint32_t s[64], dp[64];
+      tmem_ld32(lane_base + C::tS + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+      tmem_ld32(lane_base + C::tS + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      tmem_ld32(lane_base + C::tdP + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+      tmem_ld32(lane_base + C::tdP + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar->sp_free);
+      uint32_t dw[32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int col0 = wg * 64 + c * 32;
-        uint32_t s[32], dp[32];
-        tmem_ld32(lane_base + C::tS + col0, s);
-        tmem_ld32(lane_base + C::tdP + col0, dp);
-        tmem_wait_ld();
-        uint32_t dw[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float ds[2];
-#pragma unroll
-          for (int z = 0; z < 2; ++z) {
-            const bool vis = col0 + e + z < cnt;
-            const float p = vis ? ex2_mufu(fmaf(__uint_as_float(s[e + z]), sl2, -lse2)) : 0.f;
-            ds[z] = p * (__uint_as_float(dp[e + z]) - dsum);
-          }
-          dw[e / 2] = pack_bf16x2(ds[0], ds[1]);
-        }
-        st_swizzled_row32(sDS, MB * 128, r, col0, dw);
+      for (int e = 0; e < 64; e += 2) {
+        const int col = wg * 64 + e;
+        const float2 x = ffma2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sl2v, nl);
+        float2 p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+        if (col >= cnt) p.x = 0.f;
+        if (col + 1 >= cnt) p.y = 0.f;
+        const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
+        dw[e / 2] = pack_bf16x2(ds.x, ds.y);
       }
+      // dS(t-1) must have been read by its dQ MMA before this tile's dS overwrites it
+      if (t > 0) {
+        ok = mbar_wait(&bar->ds_free, static_cast<uint32_t>(t - 1) & 1u, a.status, 0x2305);
+        if (!ok) break;
+      }
+      st_swizzled_row32(sDS, MB * 128, r, wg * 64, *reinterpret_cast<uint32_t(*)[16]>(&dw[0]));
+      st_swizzled_row32(sDS, MB * 128, r, wg * 64 + 32, *reinterpret_cast<uint32_t(*)[16]>(&dw[16]));
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar->ds_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar->ds_full);
     }
     if (ok && T > 0) {
       ok = mbar_wait(&bar->acc_full, 0, a.status, 0x2310);

@@ -17,9 +17,6 @@
 // more than 8.0, in which case O and l are multiplied by 2^(m_old - m_new);
 // otherwise the stale max is kept (p <= 2^8). The epilogue divides by the
 // exact row sum, which makes the result independent of the skipped rescales.
-// Two row sums are kept: O is divided by the sum of the bf16-rounded p that the
-// P V product consumes (so the weights applied to V sum to one exactly), LSE
-// uses the sum of the unrounded fp32 p.
 // exp2 runs on the hardware unit for most columns and on the FMA pipe
 // (exp2_emu.cuh) for a fixed 1/EMU_PERIOD of them (same page, section
 // 用软件"伪造"硬件指令).
@@ -132,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < QT; ++i) {
       mbar_init(&bar->q_full[i], 1);
       mbar_init(&bar->s_full[i], 1);
-      mbar_init(&bar->p_full[i], BM);
+      mbar_init(&bar->p_full[i], 4);  // one arrival per softmax warp
       mbar_init(&bar->o_full[i], 1);
     }
     for (int s = 0; s < C::NSLOT; ++s) {
@@ -259,8 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tbase + ((quarter * 32u) << 16);
     const float sl2 = a.scale_log2;
     float m_used = -INFINITY;  // log2 units
-    float l = 0.f;   // row sum of the bf16-rounded weights (divides O)
-    float lx = 0.f;  // row sum of the fp32 weights (LSE)
+    float l = 0.f;  // row sum of the fp32 weights
     int n_rescale = 0, n_opp = 0;
     bool ok = true;
     for (int j = 0; j < nkv[i]; ++j) {
@@ -279,13 +275,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN; ++c)
           if (c >= cnt) s[c] = __float_as_uint(-INFINITY);
       }
-      // row max as 8 independent chains, then a tree (no 128-long dependency chain)
+      // row max: 8 independent chains of three-input max, then a tree
       float mp[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) mp[c] = __uint_as_float(s[c]);
+      for (int c = 0; c < 8; ++c) mp[c] = fmaxf(__uint_as_float(s[c]), __uint_as_float(s[c + 8]));
 #pragma unroll
-      for (int c = 8; c < BN; ++c) mp[c % 8] = fmaxf(mp[c % 8], __uint_as_float(s[c]));
-      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      for (int c = 16; c < BN; c += 16)
+#pragma unroll
+        for (int z = 0; z < 8; ++z) mp[z] = fmax3(mp[z], __uint_as_float(s[c + z]), __uint_as_float(s[c + 8 + z]));
+      const float mx = fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
       const float m_tile = mx * sl2;
       const bool need = m_tile > m_used + kThreshold;
       float alpha = 1.f;
@@ -298,33 +296,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         n_rescale += need;
       }
       l *= alpha;
-      lx *= alpha;
       const float mu = (m_used == -INFINITY) ? 0.f : m_used;
       // p = 2^(s * scale * log2e - m_used), packed to bf16 pairs in place
       uint32_t pk[BN / 2];
-      float2 rsp[2], rsx[2];  // partial sums: bf16-rounded p (normalises O), fp32 p (gives LSE)
-#pragma unroll
-      for (int z = 0; z < 2; ++z) rsp[z] = rsx[z] = make_float2(0.f, 0.f);
+      float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // partial row sums (packed pairs)
       const float2 sl2v = make_float2(sl2, sl2), negmu = make_float2(-mu, -mu);
 #pragma unroll
       for (int c = 0; c < BN / 2; ++c) {
         const float2 x = ffma2(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sl2v, negmu);
-        float p0, p1;
+        float2 p;
         if (EMU_PERIOD > 0 && ((2 * c) % EMU_PERIOD) == EMU_PERIOD - 2) {
-          p0 = ex2_mufu(x.x);
-          p1 = ex2_emu(x.y);
+          p = make_float2(ex2_mufu(x.x), ex2_emu(x.y));
         } else {
-          p0 = ex2_mufu(x.x);
-          p1 = ex2_mufu(x.y);
+          p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
         }
-        pk[c] = pack_bf16x2(p0, p1);
-        rsp[c % 2].x += __uint_as_float(pk[c] << 16);
-        rsp[c % 2].y += __uint_as_float(pk[c] & 0xffff0000u);
-        rsx[c % 2].x += p0;
-        rsx[c % 2].y += p1;
+        pk[c] = pack_bf16x2(p.x, p.y);
+        rs[c & 1] = fadd2(rs[c & 1], p);
       }
-      l += (rsp[0].x + rsp[0].y) + (rsp[1].x + rsp[1].y);
-      lx += (rsx[0].x + rsx[0].y) + (rsx[1].x + rsx[1].y);
+      l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
       tmem_st32(lane_base + tS(i) + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st32(lane_base + tS(i) + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       // correction: rescale this tile's O rows whose max moved (warp-uniform branch)
@@ -341,7 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bar->p_full[i]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar->p_full[i]);
     }
     if (a.stats != nullptr) {
       int r = __reduce_add_sync(0xffffffffu, n_rescale), o = __reduce_add_sync(0xffffffffu, n_opp);
@@ -380,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (store) {
-      const float lse = (lx > 0.f) ? (m_used + log2f(lx)) * 0.69314718055994531f : -INFINITY;
+      const float lse = (l > 0.f) ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
       a.lse[static_cast<int64_t>(b) * a.lse_sb + static_cast<int64_t>(h) * a.lse_sh + q_start + row] = lse;
     }
   }
@@ -415,14 +405,11 @@ __global__ void exp2_eval_kernel(const float* x, float* yp, float* yh, int64_t n
   }
 }
 
-// 1/8 of the exponentials run on the FMA pipe (the pages' 10–25% range).
-constexpr int kEmuPeriod = 8;
-
-template <int DQK, int DV>
-cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
+template <int DQK, int DV, int EMU>
+cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
                      cudaStream_t stream) {
   using C = Cfg<DQK, DV>;
-  auto kern = attn_fwd_kernel<DQK, DV, kEmuPeriod>;
+  auto kern = attn_fwd_kernel<DQK, DV, EMU>;
   static bool attr_done = false;  // benign race: the attribute calls are idempotent
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -439,6 +426,19 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
+}
+
+// exp2 split: every EMU-th column of a row goes to the FMA-pipe polynomial
+// (0 = all on the hardware unit). Built for 0, 4 and 8.
+template <int DQK, int DV>
+cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
+                     cudaStream_t stream) {
+  switch (a.emu_period) {
+    case 0: return launch_e<DQK, DV, 0>(tq, tk, tv, a, stream);
+    case 4: return launch_e<DQK, DV, 4>(tq, tk, tv, a, stream);
+    case 8: return launch_e<DQK, DV, 8>(tq, tk, tv, a, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace fwd

@@ -23,6 +23,7 @@ struct FwdArgs {
   int causal;
   uint32_t* status;          // device status word
   unsigned long long* stats; // optional rescale counters
+  int emu_period;            // exp2: every emu_period-th column on the FMA pipe (0 = none)
 };
 
 cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -74,8 +74,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status, uint32_t where) {
   if (mbar_try_wait(bar, parity)) return true;
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (i > 64) __nanosleep(64);
+    if (mbar_try_wait(bar, parity)) return true;  // try_wait itself suspends for a while
+    // Back off only after ~1M polls: sleeping earlier delays the hand-offs on
+    // the critical path (a woken MMA thread is hundreds of cycles late).
+    if (i > (1u << 20)) __nanosleep(256);
     // Another role or CTA already failed: stop waiting early (legitimate
     // waits here last microseconds, never 2^16 polls).
     if ((i & 0xFFFu) == 0xFFFu && i > (1u << 16) && status && *reinterpret_cast<volatile uint32_t*>(status) != 0)
@@ -304,6 +306,12 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
       "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
       : "=f"(d.x), "=f"(d.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
 

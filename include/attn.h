@@ -104,7 +104,13 @@ typedef struct attn_fwd_params {
   int32_t total_k;
   float softmax_scale;
   int32_t causal;
-  int32_t reserved0;
+  /* Forward only: share of exp2 computed on the FMA pipe by the Cody-Waite
+   * split + cubic instead of the hardware unit: 0 (none), 8 (one column in
+   * eight of every row) or 4 (one in four); anything else is
+   * ATTN_ERR_INVALID_ARG. The pages balance the two units for a part with
+   * half of GB300's ex2 throughput; on GB300 0 is fastest. Ignored by the
+   * backward entry points. */
+  int32_t exp2_emu_period;
   /* Optional (may be NULL): device uint64[2] to which the forward kernel adds
    * the number of conditional rescales performed after a row's first key
    * tile ([0]) and the number of such rescale opportunities ([1]). */

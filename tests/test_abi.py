@@ -89,6 +89,8 @@ INVALID, UNSUPPORTED = 1, 2
     (lambda p: setattr(p, "v_row_stride", 4 * 64 + 4), INVALID),  # not a multiple of 8
     (lambda p: setattr(p, "lse", 0x10002), INVALID),
     (lambda p: setattr(p, "cu_seqlens_q", 0x10000), INVALID),  # dense call with offsets
+    (lambda p: setattr(p, "exp2_emu_period", 3), INVALID),      # only 0, 4, 8 are built
+    (lambda p: setattr(p, "exp2_emu_period", -8), INVALID),
 ])
 def test_fwd_rejects_bad_arguments_without_a_gpu(lib, _abi, mutate, expect):
     p = _valid_fwd(_abi)

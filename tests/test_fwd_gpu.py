@@ -35,9 +35,9 @@ def ref_dense(q, k, v, scale, causal, pairs=None, row_block=4096):
     return o, lse
 
 
-def run_and_check(ea, w, pairs=None, device="cuda"):
+def run_and_check(ea, w, pairs=None, device="cuda", emu=0):
     t = workloads.make_dense(w, device=device, with_do=False)
-    o, lse = ea.attn_fwd(t["q"], t["k"], t["v"], causal=w.causal, softmax_scale=w.scale)
+    o, lse = ea.attn_fwd(t["q"], t["k"], t["v"], causal=w.causal, softmax_scale=w.scale, exp2_emu_period=emu)
     torch.cuda.synchronize()
     ea.attn_get_device_status()
     q, k, v = (t[n].cpu() for n in ("q", "k", "v"))
@@ -63,6 +63,18 @@ def test_small_shapes_full(ea, dims, causal, nq, nk):
     dqk, dv = dims
     w = workloads.Workload("small", 2, 3, nq, nk, dqk, dv, causal, seed=nq * 1000 + nk)
     run_and_check(ea, w)
+
+
+@pytest.mark.parametrize("emu", [4, 8])
+@pytest.mark.parametrize("dims", DIMS)
+@pytest.mark.parametrize("causal", [False, True])
+def test_exp2_emulation_shares(ea, emu, dims, causal):
+    # one column in `emu` of every row takes the Cody-Waite + cubic exp2 on the FMA pipe
+    dqk, dv = dims
+    w = workloads.Workload("emu", 2, 3, 300, 300, dqk, dv, causal, seed=emu)
+    run_and_check(ea, w, emu=emu)
+    w = workloads.dense_d128(4096, causal)
+    run_and_check(ea, w, pairs=workloads.sample_pairs(w.batch, w.heads, 1, seed=emu), emu=emu)
 
 
 @pytest.mark.parametrize("seqlen", workloads.DENSE_SWEEP)
