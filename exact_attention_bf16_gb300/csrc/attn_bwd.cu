@@ -109,37 +109,75 @@ __global__ void preprocess_kernel(const BwdArgs a) {
   }
 }
 
+// Copies row `row` of a K-major 128-byte-swizzled tile (64-column chunks
+// `chunk_bytes` apart) into registers as packed bf16 pairs: 32 words per chunk.
+__device__ __forceinline__ void smem_row_chunk(const uint8_t* tile, int chunk_bytes, int row, int chunk,
+                                               uint32_t (&w)[32]) {
+  const uint8_t* base = tile + chunk * chunk_bytes + row * 128;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint4 v = *reinterpret_cast<const uint4*>(base + ((u ^ (row & 7)) * 16));
+    w[4 * u] = v.x;
+    w[4 * u + 1] = v.y;
+    w[4 * u + 2] = v.z;
+    w[4 * u + 3] = v.w;
+  }
+}
+
+// Stores this thread's row of a 128-row operand tile (d columns) into TMEM as
+// an MMA A operand: lane = row, column c = elements (2c, 2c+1).
+__device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int chunks, int row, uint32_t taddr) {
+  for (int c = 0; c < chunks; ++c) {
+    uint32_t w[32];
+    smem_row_chunk(tile, KB * 128, row, c, w);
+    tmem_st32(taddr + 32 * c, w);
+  }
+}
+
 // ===========================================================================
 // dK / dV kernel (key-stationary)
 // ===========================================================================
+// Per step one 64-row query tile. S^T = K Q^T and dP^T = V dO^T go to TMEM;
+// the softmax warps turn them into P^T and dS^T (bf16 pairs) in a TMEM region
+// of their own, which feeds dV += P^T dO and dK += dS^T Q directly. Because
+// P^T/dS^T do not overwrite S^T, the next tile's S^T and dP^T are issued as
+// soon as the softmax warps have copied this tile's out of TMEM, so the
+// tensor core computes them while the softmax runs. V (and for d_qk = 64 also
+// K) sits in TMEM as an MMA A operand; the rest is read from shared memory.
 template <int DQK, int DV>
 struct DkdvCfg {
-  static constexpr int QB = DQK == 192 ? 64 : 128;  // query rows per step (TMEM budget)
+  static constexpr int QB = 64;                     // query rows per step
+  // TMEM columns: S^T | dP^T | P^T,dS^T | dV | dK | [V] | [K]
+  static constexpr uint32_t tS = 0, tdP = QB, tPdS = 2 * QB, tdV = 3 * QB, tdK = 3 * QB + DV;
+  static constexpr uint32_t BASE = tdK + DQK;
+  static constexpr bool V_TMEM = BASE + DV / 2 <= 512;
+  static constexpr uint32_t tV = BASE;
+  static constexpr uint32_t tK = BASE + (V_TMEM ? DV / 2 : 0);
+  static constexpr bool K_TMEM = tK + DQK / 2 <= 512;
   static constexpr int QCH = DQK / 64, VCH = DV / 64;
   static constexpr int K_BYTES = QCH * KB * 128;
   static constexpr int V_BYTES = VCH * KB * 128;
   static constexpr int QT_BYTES = QCH * QB * 128;   // one query tile of Q
   static constexpr int DOT_BYTES = VCH * QB * 128;  // one query tile of dO
-  static constexpr int NST = 2;
+  static constexpr int NST = 3;
   static constexpr int STAGE = QT_BYTES + DOT_BYTES;
-  static constexpr int DS_BYTES = (QB / 64) * KB * 128;  // dS^T [KB][QB] bf16, K-major
   static constexpr int OFF_V = K_BYTES;
   static constexpr int OFF_ST = OFF_V + V_BYTES;
-  static constexpr int OFF_DS = OFF_ST + NST * STAGE;
-  static constexpr int OFF_VEC = OFF_DS + DS_BYTES;          // [QB] LSE*log2e + [QB] D
-  static constexpr int OFF_BAR = OFF_VEC + 2 * QB * 4;
+  static constexpr int OFF_VEC = OFF_ST + NST * STAGE;  // [2 steps][QB] -LSE*log2e, [2 steps][QB] -D
+  static constexpr int OFF_BAR = OFF_VEC + 4 * QB * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
-  // TMEM columns
-  static constexpr uint32_t tS = 0, tdP = QB, tdV = 2 * QB, tdK = 2 * QB + DV;
-  static_assert(tdK + DQK <= 512, "TMEM budget");
+  static_assert(BASE <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct DkdvBars {
   uint64_t kv_full;
-  uint64_t st_full[2];
-  uint64_t st_empty[2];
+  uint64_t kv_tmem;
+  uint64_t st_full[3];
+  uint64_t st_empty[3];
   uint64_t s_full;
+  uint64_t sp_free;   // softmax warps hold S^T(t), dP^T(t) in registers
+  uint64_t pds_free;  // dV(t), dK(t) have read P^T(t), dS^T(t)
   uint64_t ds_full;
   uint64_t acc_full;
   uint64_t mma_done;
@@ -157,9 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::OFF_V;
   uint8_t* sST = smem + C::OFF_ST;
-  uint8_t* sDS = smem + C::OFF_DS;
-  float* sLSE = reinterpret_cast<float*>(smem + C::OFF_VEC);  // [QB]
-  float* sDv = sLSE + QB;                                      // [QB]
+  float* sLSE = reinterpret_cast<float*>(smem + C::OFF_VEC);  // [2][QB], by step parity
+  float* sDv = sLSE + 2 * QB;                                  // [2][QB]
   DkdvBars* bar = reinterpret_cast<DkdvBars*>(smem + C::OFF_BAR);
 
   // (unit, head) is the slow index so that resident CTAs share a few heads'
@@ -182,12 +219,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     mbar_init(&bar->kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    mbar_init(&bar->kv_tmem, kSoftThreads / 32);
+    for (int s = 0; s < C::NST; ++s) {
       mbar_init(&bar->st_full[s], 1);
       mbar_init(&bar->st_empty[s], 1);
     }
     mbar_init(&bar->s_full, 1);
-    mbar_init(&bar->ds_full, kSoftThreads / 32);  // one arrival per softmax warp
+    mbar_init(&bar->sp_free, kSoftThreads / 32);
+    mbar_init(&bar->pds_free, 1);
+    mbar_init(&bar->ds_full, kSoftThreads / 32);
     mbar_init(&bar->acc_full, 1);
     mbar_init(&bar->mma_done, 1);
     fence_barrier_init();
@@ -230,50 +270,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(KB, QB, false, false);  // S^T, dP^T: both operands K-major
-      constexpr uint32_t idV = idesc_bf16_f32(KB, DV, false, true);   // dV: B = dO, MN-major
-      constexpr uint32_t idK = idesc_bf16_f32(KB, DQK, false, true);  // dK: B = Q, MN-major
-      bool ok = mbar_wait(&bar->kv_full, 0, a.status, 0x1200);
-      const uint32_t kb = smem_u32(sK), vb = smem_u32(sV), dsb = smem_u32(sDS);
-      for (int t = 0; t < T && ok; ++t) {
-        const int st = t % C::NST;
-        ok = mbar_wait(&bar->st_full[st], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x1210);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t qb = smem_u32(sST + st * C::STAGE);
-        const uint32_t gb = qb + C::QT_BYTES;
-        // S^T = K Q^T   (M = 128 keys, N = QB queries, K = d_qk)
+      constexpr uint32_t idS = idesc_bf16_f32(KB, QB, false, false);  // S^T, dP^T: B = Q / dO tile, K-major
+      constexpr uint32_t idV = idesc_bf16_f32(KB, DV, false, true);   // dV: B = dO tile, MN-major
+      constexpr uint32_t idK = idesc_bf16_f32(KB, DQK, false, true);  // dK: B = Q tile, MN-major
+      bool ok = mbar_wait(&bar->kv_tmem, 0, a.status, 0x1200);
+      const uint32_t kb = smem_u32(sK);
+      auto stage_q = [&](int t) { return smem_u32(sST + (t % C::NST) * C::STAGE); };
+      auto wait_stage = [&](int t) {
+        return mbar_wait(&bar->st_full[t % C::NST], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x1210);
+      };
+      auto issue_s = [&](int t) {  // S^T = K Q^T  (M = 128 keys, N = 64 queries, K = d_qk)
+        const uint32_t qb = stage_q(t);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint64_t ad = smem_desc(kb + (kk / 4) * KB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
           const uint64_t bd = smem_desc(qb + (kk / 4) * QB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
-          mma_ss(tbase + C::tS, ad, bd, idS, kk > 0 ? 1u : 0u);
+          if constexpr (C::K_TMEM) {
+            mma_ts(tbase + C::tS, tbase + C::tK + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
+          } else {
+            const uint64_t ad = smem_desc(kb + (kk / 4) * KB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
+            mma_ss(tbase + C::tS, ad, bd, idS, kk > 0 ? 1u : 0u);
+          }
         }
-        // dP^T = V dO^T  (K = d_v)
+      };
+      const uint32_t vb = smem_u32(sV);
+      auto issue_dp = [&](int t) {  // dP^T = V dO^T  (K = d_v)
+        const uint32_t gb = stage_q(t) + C::QT_BYTES;
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
-          const uint64_t ad = smem_desc(vb + (kk / 4) * KB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
           const uint64_t bd = smem_desc(gb + (kk / 4) * QB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
-          mma_ss(tbase + C::tdP, ad, bd, idS, kk > 0 ? 1u : 0u);
+          if constexpr (C::V_TMEM) {
+            mma_ts(tbase + C::tdP, tbase + C::tV + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
+          } else {
+            const uint64_t ad = smem_desc(vb + (kk / 4) * KB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
+            mma_ss(tbase + C::tdP, ad, bd, idS, kk > 0 ? 1u : 0u);
+          }
         }
-        mma_commit(&bar->s_full);
+      };
+      if (ok) ok = mbar_wait(&bar->kv_full, 0, a.status, 0x1201);
+      if (ok && T > 0) {
+        ok = wait_stage(0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+          issue_dp(0);
+          mma_commit(&bar->s_full);
+        }
+      }
+      for (int t = 0; t < T && ok; ++t) {
+        if (t + 1 < T) {  // next S^T, dP^T as soon as the softmax warps hold this tile's
+          ok = mbar_wait(&bar->sp_free, static_cast<uint32_t>(t) & 1u, a.status, 0x1215) && wait_stage(t + 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(t + 1);
+          issue_dp(t + 1);
+          mma_commit(&bar->s_full);
+        }
         ok = mbar_wait(&bar->ds_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1220);
         if (!ok) break;
         tc_fence_after();
-        // dV += P^T dO  (A = P^T from TMEM: 16 packed columns per 32-query chunk)
+        const uint32_t qb = stage_q(t), gb = qb + C::QT_BYTES;
+        // dV += P^T dO and dK += dS^T Q, A from TMEM: warpgroup w's 32 queries are
+        // in columns tPdS + [32w, 32w+32): P^T in the first 16, dS^T in the last 16
 #pragma unroll
         for (int kk = 0; kk < QB / 16; ++kk) {
-          const uint64_t bd = smem_desc(gb + kk * 2048, QB * 128, 1024, SWZ_128B);
-          mma_ts(tbase + C::tdV, tbase + C::tS + (kk / 2) * 32 + (kk % 2) * 8, bd, idV, (t > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t pa = tbase + C::tPdS + 32 * (kk / 2) + (kk % 2) * 8;
+          mma_ts(tbase + C::tdV, pa, smem_desc(gb + kk * 2048, QB * 128, 1024, SWZ_128B), idV,
+                 (t > 0 || kk > 0) ? 1u : 0u);
         }
-        // dK += dS^T Q  (A = dS^T in shared memory, K-major)
 #pragma unroll
         for (int kk = 0; kk < QB / 16; ++kk) {
-          const uint64_t ad = smem_desc(dsb + (kk / 4) * KB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
-          const uint64_t bd = smem_desc(qb + kk * 2048, QB * 128, 1024, SWZ_128B);
-          mma_ss(tbase + C::tdK, ad, bd, idK, (t > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t da = tbase + C::tPdS + 32 * (kk / 2) + 16 + (kk % 2) * 8;
+          mma_ts(tbase + C::tdK, da, smem_desc(qb + kk * 2048, QB * 128, 1024, SWZ_128B), idK,
+                 (t > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&bar->st_empty[st]);
+        mma_commit(&bar->pds_free);
+        mma_commit(&bar->st_empty[t % C::NST]);
       }
       mma_commit(&bar->acc_full);
       mma_commit(&bar->mma_done);
@@ -281,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ================= softmax gradient: one key row per thread ============
-    const int wg = static_cast<int>(warp) / 4;           // which half of the query columns
+    const int wg = static_cast<int>(warp) / 4;           // which 32 of the 64 query columns
     const uint32_t quarter = warp & 3u;
     const int j = static_cast<int>(quarter * 32 + lane);  // key row within the tile
     const int kj = k0 + j;                                // key index within the sequence
@@ -290,61 +361,92 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i_vis = a.causal ? kj - (U.nk - U.nq) : -0x40000000;
     const bool key_ok = kj < U.nk;
     const float sl2 = a.scale_log2;
-    constexpr int CPW = QB / 2;  // query columns per warpgroup
-    bool ok = true;
+    const uint32_t my_cols = C::tS + 32 * wg;     // this warpgroup's S^T columns
+    const uint32_t my_pds = C::tPdS + 32 * wg;    // its P^T (16) and dS^T (16) columns
+    bool ok = mbar_wait(&bar->kv_full, 0, a.status, 0x1301);
+    // K (warpgroup 0) and V (warpgroup 1) rows into TMEM as MMA A operands, where they fit
+    if (ok) {
+      if (wg == 0) {
+        if constexpr (C::K_TMEM) tile_row_to_tmem(sK, C::QCH, j, lane_base + C::tK);
+      } else {
+        if constexpr (C::V_TMEM) tile_row_to_tmem(sV, C::VCH, j, lane_base + C::tV);
+      }
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar->kv_tmem);
+    const float2 sl2v = make_float2(sl2, sl2);
+    // Per query tile the softmax needs -LSE*log2e and -D of its 64 queries.
+    // Threads 0..127 fetch them from global memory two steps ahead (registers)
+    // and publish them one step ahead into a smem buffer chosen by step parity,
+    // so no global-memory latency sits on a step's critical path.
+    const int tid = static_cast<int>(threadIdx.x);  // 0..255
+    auto fetch = [&](int t) -> float {
+      const int q = (m_begin + t) * QB + (tid & (QB - 1));
+      if (tid < QB) {
+        float v = INFINITY;
+        if (q < U.nq) {
+          const float l = a.lse[U.b * a.lse_sb + h * a.lse_sh + U.q_start + q];
+          v = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+        }
+        return -v;  // P = 2^(S * scale * log2e + this)
+      }
+      return (q < U.nq) ? -a.dsum[U.b * a.lse_sb + h * a.lse_sh + U.q_start + q] : 0.f;  // -D
+    };
+    auto publish = [&](int t, float v) {
+      if (tid < QB) sLSE[(t & 1) * QB + tid] = v;
+      else if (tid < 2 * QB) sDv[(t & 1) * QB + tid - QB] = v;
+    };
+    float pref = 0.f;
+    if (tid < 2 * QB && T > 0) {
+      publish(0, fetch(0));
+      if (T > 1) pref = fetch(1);
+    }
     for (int t = 0; t < T; ++t) {
       const int q0 = (m_begin + t) * QB;
-      {
-        const int tid = static_cast<int>(threadIdx.x);  // 0..255
-        named_bar_sync(1, kSoftThreads);  // everyone is done reading the previous step's vectors
-        if (tid < QB) {
-          const int i = q0 + tid;
-          float v = INFINITY;
-          if (i < U.nq) {
-            const float l = a.lse[U.b * a.lse_sb + h * a.lse_sh + U.q_start + i];
-            v = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
-          }
-          sLSE[tid] = -v;  // stored negated: P = 2^(S * scale * log2e + sLSE)
-        } else if (tid < 2 * QB) {
-          const int i = q0 + tid - QB;
-          sDv[tid - QB] = (i < U.nq) ? -a.dsum[U.b * a.lse_sb + h * a.lse_sh + U.q_start + i] : 0.f;  // -D
-        }
-        named_bar_sync(1, kSoftThreads);
-      }
-      ok = mbar_wait(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1300);
+      // everyone is done with step t-1 (so buffer (t+1)&1 is free) and step t's
+      // vectors are visible; a failed wait anywhere ends every loop here
+      ok = bar_and(1, kSoftThreads, ok);
       if (!ok) break;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < CPW / 32; ++c) {
-        const int col0 = wg * CPW + c * 32;
-        uint32_t s[32], dp[32];
-        tmem_ld32(lane_base + C::tS + col0, s);
-        tmem_ld32(lane_base + C::tdP + col0, dp);
-        tmem_wait_ld();
-        uint32_t pw[16], dw[16];
-        const float2 sl2v = make_float2(sl2, sl2);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int col = col0 + e;
-          // smem holds -LSE*log2e and -D per query column (broadcast reads)
-          const float2 nl = *reinterpret_cast<const float2*>(&sLSE[col]);
-          const float2 nd = *reinterpret_cast<const float2*>(&sDv[col]);
-          const float2 x = ffma2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sl2v, nl);
-          float2 p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
-          if (!(key_ok && q0 + col >= i_vis)) p.x = 0.f;
-          if (!(key_ok && q0 + col + 1 >= i_vis)) p.y = 0.f;
-          const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
-          pw[e / 2] = pack_bf16x2(p.x, p.y);
-          dw[e / 2] = pack_bf16x2(ds.x, ds.y);
-        }
-        // P^T for these 32 queries goes to the first 16 columns of the S
-        // columns this thread just read (never into columns the other
-        // warpgroup has yet to read).
-        tmem_st16(lane_base + C::tS + col0, pw);
-        st_swizzled_row32(sDS, KB * 128, j, col0, dw);
+      if (tid < 2 * QB && t + 1 < T) {
+        publish(t + 1, pref);
+        if (t + 2 < T) pref = fetch(t + 2);
       }
+      const float* vLSE = sLSE + (t & 1) * QB;
+      const float* vD = sDv + (t & 1) * QB;
+      ok = mbar_wait(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1300);
+      if (!ok) continue;  // leave at the next collective barrier
+      tc_fence_after();
+      uint32_t s[32], dp[32];
+      tmem_ld32(lane_base + my_cols, s);
+      tmem_ld32(lane_base + C::tdP + 32 * wg, dp);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar->sp_free);
+      uint32_t pw[16], dw[16];
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        const int col = 32 * wg + e;
+        const float2 nl = *reinterpret_cast<const float2*>(&vLSE[col]);
+        const float2 nd = *reinterpret_cast<const float2*>(&vD[col]);
+        const float2 x = ffma2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sl2v, nl);
+        float2 p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+        if (!(key_ok && q0 + col >= i_vis)) p.x = 0.f;
+        if (!(key_ok && q0 + col + 1 >= i_vis)) p.y = 0.f;
+        const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
+        pw[e / 2] = pack_bf16x2(p.x, p.y);
+        dw[e / 2] = pack_bf16x2(ds.x, ds.y);
+      }
+      if (t > 0) {  // dV(t-1), dK(t-1) must have read the previous P^T, dS^T
+        ok = mbar_wait(&bar->pds_free, static_cast<uint32_t>(t - 1) & 1u, a.status, 0x1305);
+        if (!ok) continue;
+        tc_fence_after();
+      }
+      tmem_st16(lane_base + my_pds, pw);
+      tmem_st16(lane_base + my_pds + 16, dw);
       tmem_wait_st();
-      fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar->ds_full);
@@ -398,8 +500,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===========================================================================
 // dQ kernel (query-stationary)
 // ===========================================================================
+// S = Q K^T and dP = dO V^T go to TMEM; the softmax warps write dS (bf16
+// pairs) to a TMEM region of its own that feeds dQ += dS K directly. Because
+// dS does not overwrite S, the next tile's S and dP are issued as soon as the
+// softmax warps have copied this tile's out of TMEM. dO sits in TMEM as the A
+// operand of dP where it fits (d_qk <= 128); Q is read from shared memory.
 template <int DQK, int DV>
 struct DqCfg {
+  static constexpr bool DO_TMEM = DQK <= 128;
   static constexpr int QCH = DQK / 64, VCH = DV / 64;
   static constexpr int Q_BYTES = QCH * MB * 128;
   static constexpr int DO_BYTES = VCH * MB * 128;
@@ -407,24 +515,24 @@ struct DqCfg {
   static constexpr int V_BYTES = VCH * KB * 128;
   static constexpr int NST = DQK == 192 ? 1 : 2;
   static constexpr int STAGE = K_BYTES + V_BYTES;
-  static constexpr int DS_BYTES = 2 * MB * 128;  // dS [MB][KB] bf16, K-major
   static constexpr int OFF_DO = Q_BYTES;
   static constexpr int OFF_ST = OFF_DO + DO_BYTES;
-  static constexpr int OFF_DS = OFF_ST + NST * STAGE;
-  static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
+  static constexpr int OFF_BAR = OFF_ST + NST * STAGE;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
-  static constexpr uint32_t tS = 0, tdP = 128, tdQ = 256;
-  static_assert(tdQ + DQK <= 512, "TMEM budget");
+  // TMEM columns: S | dP | dS | dQ | [dO]
+  static constexpr uint32_t tS = 0, tdP = 128, tdS = 256, tdQ = 320, tdO = 320 + DQK;
+  static_assert(tdO + (DO_TMEM ? DV / 2 : 0) <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct DqBars {
   uint64_t q_full;
+  uint64_t qd_tmem;
   uint64_t st_full[2];
   uint64_t st_empty[2];
   uint64_t s_full;
-  uint64_t sp_free;   // softmax warps hold S(t), dP(t) in registers: TMEM may be overwritten
-  uint64_t ds_free;   // dQ(t) has read dS(t) from shared memory
+  uint64_t sp_free;   // softmax warps hold S(t), dP(t) in registers
+  uint64_t ds_free;   // dQ(t) has read dS(t)
   uint64_t ds_full;
   uint64_t acc_full;
   uint64_t mma_done;
@@ -447,7 +555,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = smem;
   uint8_t* sdO = smem + C::OFF_DO;
   uint8_t* sST = smem + C::OFF_ST;
-  uint8_t* sDS = smem + C::OFF_DS;
   DqBars* bar = reinterpret_cast<DqBars*>(smem + C::OFF_BAR);
 
   // (unit, head) slow for L2 sharing of K/V; heaviest (last) query tiles first within a head
@@ -463,6 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
+    mbar_init(&bar->qd_tmem, kSoftThreads / 32);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar->st_full[s], 1);
       mbar_init(&bar->st_empty[s], 1);
@@ -515,56 +623,75 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(MB, KB, false, false);
       constexpr uint32_t idQ = idesc_bf16_f32(MB, DQK, false, true);  // B = K tile, MN-major
-      bool ok = mbar_wait(&bar->q_full, 0, a.status, 0x2200);
-      const uint32_t qb = smem_u32(sQ), gb = smem_u32(sdO), dsb = smem_u32(sDS);
-      // S(t) = Q K_t^T and dP(t) = dO V_t^T into TMEM, then signal the softmax warps.
-      auto issue_s_dp = [&](int t) -> bool {
-        const int st = t % C::NST;
-        if (!mbar_wait(&bar->st_full[st], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x2210)) return false;
-        tc_fence_after();
-        const uint32_t kb = smem_u32(sST + st * C::STAGE);
-        const uint32_t vb = kb + C::K_BYTES;
+      bool ok = mbar_wait(&bar->qd_tmem, 0, a.status, 0x2200);
+      const uint32_t qb = smem_u32(sQ);
+      auto stage_k = [&](int t) { return smem_u32(sST + (t % C::NST) * C::STAGE); };
+      auto wait_stage = [&](int t) {
+        return mbar_wait(&bar->st_full[t % C::NST], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x2210);
+      };
+      const uint32_t gb = smem_u32(sdO);
+      auto issue_s = [&](int t) {  // S = Q K^T
+        const uint32_t kb = stage_k(t);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint32_t off = (kk / 4) * MB * 128 + (kk % 4) * 32;
+          const uint32_t off = (kk / 4) * KB * 128 + (kk % 4) * 32;
           mma_ss(tbase + C::tS, smem_desc(qb + off, 16, 1024, SWZ_128B), smem_desc(kb + off, 16, 1024, SWZ_128B), idS,
                  kk > 0 ? 1u : 0u);
         }
+      };
+      auto issue_dp = [&](int t) {  // dP = dO V^T
+        const uint32_t vb = stage_k(t) + C::K_BYTES;
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
-          const uint32_t off = (kk / 4) * MB * 128 + (kk % 4) * 32;
-          mma_ss(tbase + C::tdP, smem_desc(gb + off, 16, 1024, SWZ_128B), smem_desc(vb + off, 16, 1024, SWZ_128B),
-                 idS, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk / 4) * KB * 128 + (kk % 4) * 32;
+          const uint64_t bd = smem_desc(vb + off, 16, 1024, SWZ_128B);
+          if constexpr (C::DO_TMEM) {
+            mma_ts(tbase + C::tdP, tbase + C::tdO + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
+          } else {
+            mma_ss(tbase + C::tdP, smem_desc(gb + off, 16, 1024, SWZ_128B), bd, idS, kk > 0 ? 1u : 0u);
+          }
         }
-        mma_commit(&bar->s_full);
-        return true;
       };
-      if (ok && T > 0) ok = issue_s_dp(0);
+      if (ok) ok = mbar_wait(&bar->q_full, 0, a.status, 0x2201);
+      if (ok && T > 0) {
+        ok = wait_stage(0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+          issue_dp(0);
+          mma_commit(&bar->s_full);
+        }
+      }
       for (int t = 0; t < T && ok; ++t) {
-        const int st = t % C::NST;
-        // With two K/V stages the next tile's S and dP are computed while the
-        // softmax warps work on this one (they have already copied S(t), dP(t)).
-        if (C::NST > 1 && t + 1 < T) {
-          ok = mbar_wait(&bar->sp_free, static_cast<uint32_t>(t) & 1u, a.status, 0x2215);
-          if (ok) ok = issue_s_dp(t + 1);
+        if (C::NST > 1 && t + 1 < T) {  // next S, dP as soon as the softmax warps hold this tile's
+          ok = mbar_wait(&bar->sp_free, static_cast<uint32_t>(t) & 1u, a.status, 0x2215) && wait_stage(t + 1);
           if (!ok) break;
+          tc_fence_after();
+          issue_s(t + 1);
+          issue_dp(t + 1);
+          mma_commit(&bar->s_full);
         }
         ok = mbar_wait(&bar->ds_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2220);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t kb = smem_u32(sST + st * C::STAGE);
+        const uint32_t kb = stage_k(t);
+        // dQ += dS K: A = dS from TMEM (warpgroup w's 64 keys in columns tdS + [32w, 32w+32)),
+        // B = K tile read as [d][kv], MN-major
 #pragma unroll
-        for (int kk = 0; kk < KB / 16; ++kk) {  // dQ += dS K   (B = K tile as [d][kv], MN-major)
-          const uint64_t ad = smem_desc(dsb + (kk / 4) * MB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
-          const uint64_t bd = smem_desc(kb + kk * 2048, KB * 128, 1024, SWZ_128B);
-          mma_ss(tbase + C::tdQ, ad, bd, idQ, (t > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < KB / 16; ++kk) {
+          const uint32_t da = tbase + C::tdS + 32 * (kk / 4) + (kk % 4) * 8;
+          mma_ts(tbase + C::tdQ, da, smem_desc(kb + kk * 2048, KB * 128, 1024, SWZ_128B), idQ,
+                 (t > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&bar->ds_free);
-        mma_commit(&bar->st_empty[st]);
-        if (C::NST == 1 && t + 1 < T) {
-          // one stage: the next K/V tile can only arrive after this dQ has read K(t)
-          ok = issue_s_dp(t + 1);
+        mma_commit(&bar->st_empty[t % C::NST]);
+        if (C::NST == 1 && t + 1 < T) {  // one stage: the next K/V tile arrives only after this dQ has read K(t)
+          ok = wait_stage(t + 1);
           if (!ok) break;
+          tc_fence_after();
+          issue_s(t + 1);
+          issue_dp(t + 1);
+          mma_commit(&bar->s_full);
         }
       }
       mma_commit(&bar->acc_full);
@@ -586,14 +713,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       dsum = a.dsum[U.b * a.lse_sb + h * a.lse_sh + U.q_start + i];
     }
     const float sl2 = a.scale_log2;
-    bool ok = true;
+    bool ok = mbar_wait(&bar->q_full, 0, a.status, 0x2301);
+    // dO rows into TMEM as the A operand of dP, where it fits
+    if (ok && wg == 1) {
+      if constexpr (C::DO_TMEM) tile_row_to_tmem(sdO, C::VCH, r, lane_base + C::tdO);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar->qd_tmem);
     const float2 sl2v = make_float2(sl2, sl2), nl = make_float2(-lse2, -lse2), nd = make_float2(-dsum, -dsum);
-    for (int t = 0; t < T; ++t) {
+    for (int t = 0; t < T && ok; ++t) {
       ok = mbar_wait(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2300);
       if (!ok) break;
       tc_fence_after();
       const int cnt = lim - t * KB;  // visible keys of this row in tile t
-      // copy this warpgroup's 64 columns of S and dP out of TMEM, then release them
+      // copy this warpgroup's 64 columns of S and dP out of TMEM, then release dP
       uint32_t s[64], dp[64];
       tmem_ld32(lane_base + C::tS + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
       tmem_ld32(lane_base + C::tS + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
@@ -614,14 +749,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
         dw[e / 2] = pack_bf16x2(ds.x, ds.y);
       }
-      // dS(t-1) must have been read by its dQ MMA before this tile's dS overwrites it
-      if (t > 0) {
+      if (t > 0) {  // dQ(t-1) must have read the previous dS
         ok = mbar_wait(&bar->ds_free, static_cast<uint32_t>(t - 1) & 1u, a.status, 0x2305);
         if (!ok) break;
+        tc_fence_after();
       }
-      st_swizzled_row32(sDS, MB * 128, r, wg * 64, *reinterpret_cast<uint32_t(*)[16]>(&dw[0]));
-      st_swizzled_row32(sDS, MB * 128, r, wg * 64 + 32, *reinterpret_cast<uint32_t(*)[16]>(&dw[16]));
-      fence_async_smem();
+      tmem_st32(lane_base + C::tdS + wg * 32, dw);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar->ds_full);
@@ -711,7 +845,6 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 
 }  // namespace bwd
 
-int bwd_dkdv_query_rows(int d_qk) { return d_qk == 192 ? 64 : 128; }
 
 cudaError_t launch_bwd_preprocess(int d_v, const BwdArgs& a, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(a.batch) * a.seqlen_q * a.heads;

@@ -275,6 +275,24 @@ __device__ __forceinline__ void regs_inc() {
 }
 
 // ---------------------------------------------------------------------------
+// Named barrier over `n` threads that also ANDs a per-thread flag, so a
+// give-up decision is taken by every participant together (no thread is left
+// waiting at a barrier the others will not reach).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool bar_and(int id, int n, bool flag) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.cta.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(flag ? 1u : 0u), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// ---------------------------------------------------------------------------
 // Small numeric helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
