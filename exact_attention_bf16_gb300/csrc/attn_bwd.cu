@@ -163,8 +163,8 @@ struct DkdvCfg {
   static constexpr int STAGE = QT_BYTES + DOT_BYTES;
   static constexpr int OFF_V = K_BYTES;
   static constexpr int OFF_ST = OFF_V + V_BYTES;
-  static constexpr int OFF_VEC = OFF_ST + NST * STAGE;  // [2 steps][QB] -LSE*log2e, [2 steps][QB] -D
-  static constexpr int OFF_BAR = OFF_VEC + 4 * QB * 4;
+  static constexpr int OFF_VEC = OFF_ST + NST * STAGE;  // per stage: [QB] -LSE*log2e, [QB] -D
+  static constexpr int OFF_BAR = OFF_VEC + NST * 2 * QB * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static_assert(BASE <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -195,8 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::OFF_V;
   uint8_t* sST = smem + C::OFF_ST;
-  float* sLSE = reinterpret_cast<float*>(smem + C::OFF_VEC);  // [2][QB], by step parity
-  float* sDv = sLSE + 2 * QB;                                  // [2][QB]
+  float* sVec = reinterpret_cast<float*>(smem + C::OFF_VEC);  // [NST][2][QB], beside the stages
   DkdvBars* bar = reinterpret_cast<DkdvBars*>(smem + C::OFF_BAR);
 
   // (unit, head) is the slow index so that resident CTAs share a few heads'
@@ -221,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar->kv_full, 1);
     mbar_init(&bar->kv_tmem, kSoftThreads / 32);
     for (int s = 0; s < C::NST; ++s) {
-      mbar_init(&bar->st_full[s], 1);
+      mbar_init(&bar->st_full[s], 1 + 32);  // the TMA bytes plus one arrival per loader lane
       mbar_init(&bar->st_empty[s], 1);
     }
     mbar_init(&bar->s_full, 1);
@@ -248,21 +247,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(sK + c * KB * 128, &tmk, &bar->kv_full, c * 64, h, U.k_start + k0, U.b);
       for (int c = 0; c < C::VCH; ++c)
         tma_load_4d(sV + c * KB * 128, &tmv, &bar->kv_full, c * 64, h, U.k_start + k0, U.b);
-      int issued = 0;
-      bool ok = true;
-      for (int t = 0; t < T && ok; ++t) {
-        const int st = t % C::NST;
-        const uint32_t use = static_cast<uint32_t>(t / C::NST);
-        ok = mbar_wait(&bar->st_empty[st], (use & 1u) ^ 1u, a.status, 0x1100 + st);
-        if (!ok) break;
+    }
+    // Lane 0 streams the Q and dO tiles; every lane also writes two of the
+    // tile's 64 (-LSE*log2e, -D) pairs next to the stage and arrives on the
+    // stage's barrier, so the softmax warps find them there with no barrier
+    // of their own (the slot is recycled only after dV, dK of that tile ran).
+    int issued = 0;
+    bool ok = true;
+    for (int t = 0; t < T && ok; ++t) {
+      const int st = t % C::NST;
+      const uint32_t use = static_cast<uint32_t>(t / C::NST);
+      ok = mbar_wait(&bar->st_empty[st], (use & 1u) ^ 1u, a.status, 0x1100 + st);
+      if (!ok) break;
+      const int tile = (m_begin + t) * QB;
+      if (lane == 0) {
         uint8_t* dst = sST + st * C::STAGE;
-        const int row = U.q_start + (m_begin + t) * QB;
+        const int row = U.q_start + tile;
         mbar_arrive_expect_tx(&bar->st_full[st], C::STAGE);
         for (int c = 0; c < C::QCH; ++c) tma_load_4d(dst + c * QB * 128, &tmq, &bar->st_full[st], c * 64, h, row, U.b);
         for (int c = 0; c < C::VCH; ++c)
           tma_load_4d(dst + C::QT_BYTES + c * QB * 128, &tmdo, &bar->st_full[st], c * 64, h, row, U.b);
-        ++issued;
       }
+      float* vec = sVec + st * 2 * QB;
+#pragma unroll
+      for (int r = static_cast<int>(lane); r < QB; r += 32) {
+        float nl = -INFINITY, nd = 0.f;  // rows past the end: P = 0
+        if (tile + r < U.nq) {
+          const int64_t idx = U.b * a.lse_sb + h * a.lse_sh + U.q_start + tile + r;
+          const float l = a.lse[idx];
+          nl = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;  // P = 2^(S * scale * log2e + nl)
+          nd = -a.dsum[idx];
+        }
+        vec[r] = nl;
+        vec[QB + r] = nd;
+      }
+      mbar_arrive(&bar->st_full[st]);
+      ++issued;
+    }
+    if (lane == 0) {
       if (!ok)
         for (int t = issued - 1; t >= 0 && t >= issued - C::NST; --t)
           mbar_wait(&bar->st_full[t % C::NST], static_cast<uint32_t>(t / C::NST) & 1u, nullptr, 0);
@@ -279,30 +301,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait_stage = [&](int t) {
         return mbar_wait(&bar->st_full[t % C::NST], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x1210);
       };
+      // Descriptors are built once (K, V) or once per tile (Q, dO) and advanced
+      // per k-step with desc_add, which keeps the single issuing thread's
+      // instruction stream short between MMAs.
+      const uint64_t dK = smem_desc(kb, 16, 1024, SWZ_128B);
+      const uint64_t dV0 = smem_desc(smem_u32(sV), 16, 1024, SWZ_128B);
       auto issue_s = [&](int t) {  // S^T = K Q^T  (M = 128 keys, N = 64 queries, K = d_qk)
-        const uint32_t qb = stage_q(t);
+        const uint64_t dq = smem_desc(stage_q(t), 16, 1024, SWZ_128B);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
-          const uint64_t bd = smem_desc(qb + (kk / 4) * QB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
+          const uint64_t bd = desc_add(dq, (kk / 4) * QB * 128 + (kk % 4) * 32);
           if constexpr (C::K_TMEM) {
             mma_ts(tbase + C::tS, tbase + C::tK + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
           } else {
-            const uint64_t ad = smem_desc(kb + (kk / 4) * KB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
-            mma_ss(tbase + C::tS, ad, bd, idS, kk > 0 ? 1u : 0u);
+            mma_ss(tbase + C::tS, desc_add(dK, (kk / 4) * KB * 128 + (kk % 4) * 32), bd, idS, kk > 0 ? 1u : 0u);
           }
         }
       };
-      const uint32_t vb = smem_u32(sV);
       auto issue_dp = [&](int t) {  // dP^T = V dO^T  (K = d_v)
-        const uint32_t gb = stage_q(t) + C::QT_BYTES;
+        const uint64_t dg = smem_desc(stage_q(t) + C::QT_BYTES, 16, 1024, SWZ_128B);
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
-          const uint64_t bd = smem_desc(gb + (kk / 4) * QB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
+          const uint64_t bd = desc_add(dg, (kk / 4) * QB * 128 + (kk % 4) * 32);
           if constexpr (C::V_TMEM) {
             mma_ts(tbase + C::tdP, tbase + C::tV + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
           } else {
-            const uint64_t ad = smem_desc(vb + (kk / 4) * KB * 128 + (kk % 4) * 32, 16, 1024, SWZ_128B);
-            mma_ss(tbase + C::tdP, ad, bd, idS, kk > 0 ? 1u : 0u);
+            mma_ss(tbase + C::tdP, desc_add(dV0, (kk / 4) * KB * 128 + (kk % 4) * 32), bd, idS, kk > 0 ? 1u : 0u);
           }
         }
       };
@@ -328,20 +352,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&bar->ds_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1220);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t qb = stage_q(t), gb = qb + C::QT_BYTES;
+        const uint64_t mq = smem_desc(stage_q(t), QB * 128, 1024, SWZ_128B);           // Q tile, MN-major
+        const uint64_t mg = smem_desc(stage_q(t) + C::QT_BYTES, QB * 128, 1024, SWZ_128B);  // dO tile, MN-major
+        const uint32_t acc0 = t > 0 ? 1u : 0u;
         // dV += P^T dO and dK += dS^T Q, A from TMEM: warpgroup w's 32 queries are
         // in columns tPdS + [32w, 32w+32): P^T in the first 16, dS^T in the last 16
 #pragma unroll
         for (int kk = 0; kk < QB / 16; ++kk) {
           const uint32_t pa = tbase + C::tPdS + 32 * (kk / 2) + (kk % 2) * 8;
-          mma_ts(tbase + C::tdV, pa, smem_desc(gb + kk * 2048, QB * 128, 1024, SWZ_128B), idV,
-                 (t > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tbase + C::tdV, pa, desc_add(mg, kk * 2048), idV, kk > 0 ? 1u : acc0);
         }
 #pragma unroll
         for (int kk = 0; kk < QB / 16; ++kk) {
           const uint32_t da = tbase + C::tPdS + 32 * (kk / 2) + 16 + (kk % 2) * 8;
-          mma_ts(tbase + C::tdK, da, smem_desc(qb + kk * 2048, QB * 128, 1024, SWZ_128B), idK,
-                 (t > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tbase + C::tdK, da, desc_add(mq, kk * 2048), idK, kk > 0 ? 1u : acc0);
         }
         mma_commit(&bar->pds_free);
         mma_commit(&bar->st_empty[t % C::NST]);
@@ -377,47 +401,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar->kv_tmem);
     const float2 sl2v = make_float2(sl2, sl2);
-    // Per query tile the softmax needs -LSE*log2e and -D of its 64 queries.
-    // Threads 0..127 fetch them from global memory two steps ahead (registers)
-    // and publish them one step ahead into a smem buffer chosen by step parity,
-    // so no global-memory latency sits on a step's critical path.
-    const int tid = static_cast<int>(threadIdx.x);  // 0..255
-    auto fetch = [&](int t) -> float {
-      const int q = (m_begin + t) * QB + (tid & (QB - 1));
-      if (tid < QB) {
-        float v = INFINITY;
-        if (q < U.nq) {
-          const float l = a.lse[U.b * a.lse_sb + h * a.lse_sh + U.q_start + q];
-          v = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
-        }
-        return -v;  // P = 2^(S * scale * log2e + this)
-      }
-      return (q < U.nq) ? -a.dsum[U.b * a.lse_sb + h * a.lse_sh + U.q_start + q] : 0.f;  // -D
-    };
-    auto publish = [&](int t, float v) {
-      if (tid < QB) sLSE[(t & 1) * QB + tid] = v;
-      else if (tid < 2 * QB) sDv[(t & 1) * QB + tid - QB] = v;
-    };
-    float pref = 0.f;
-    if (tid < 2 * QB && T > 0) {
-      publish(0, fetch(0));
-      if (T > 1) pref = fetch(1);
-    }
-    for (int t = 0; t < T; ++t) {
+    for (int t = 0; t < T && ok; ++t) {
       const int q0 = (m_begin + t) * QB;
-      // everyone is done with step t-1 (so buffer (t+1)&1 is free) and step t's
-      // vectors are visible; a failed wait anywhere ends every loop here
-      ok = bar_and(1, kSoftThreads, ok);
-      if (!ok) break;
-      if (tid < 2 * QB && t + 1 < T) {
-        publish(t + 1, pref);
-        if (t + 2 < T) pref = fetch(t + 2);
-      }
-      const float* vLSE = sLSE + (t & 1) * QB;
-      const float* vD = sDv + (t & 1) * QB;
       ok = mbar_wait(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1300);
-      if (!ok) continue;  // leave at the next collective barrier
+      // this tile's (-LSE*log2e, -D) vectors, written by the loader lanes
+      if (ok) ok = mbar_wait(&bar->st_full[t % C::NST], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x1302);
+      if (!ok) break;
       tc_fence_after();
+      const float* vL = sVec + (t % C::NST) * 2 * QB + 32 * wg;
+      const float* vD = vL + QB;
       uint32_t s[32], dp[32];
       tmem_ld32(lane_base + my_cols, s);
       tmem_ld32(lane_base + C::tdP + 32 * wg, dp);
@@ -426,22 +418,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar->sp_free);
       uint32_t pw[16], dw[16];
-#pragma unroll
-      for (int e = 0; e < 32; e += 2) {
+      auto pair = [&](int e, float2 nl, float2 nd, bool mask) {
         const int col = 32 * wg + e;
-        const float2 nl = *reinterpret_cast<const float2*>(&vLSE[col]);
-        const float2 nd = *reinterpret_cast<const float2*>(&vD[col]);
         const float2 x = ffma2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sl2v, nl);
         float2 p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
-        if (!(key_ok && q0 + col >= i_vis)) p.x = 0.f;
-        if (!(key_ok && q0 + col + 1 >= i_vis)) p.y = 0.f;
+        if (mask) {
+          if (!(key_ok && q0 + col >= i_vis)) p.x = 0.f;
+          if (!(key_ok && q0 + col + 1 >= i_vis)) p.y = 0.f;
+        }
         const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
         pw[e / 2] = pack_bf16x2(p.x, p.y);
         dw[e / 2] = pack_bf16x2(ds.x, ds.y);
-      }
+      };
+      auto row = [&](bool mask) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 nl = *reinterpret_cast<const float4*>(vL + e);
+          const float4 nd = *reinterpret_cast<const float4*>(vD + e);
+          pair(e, make_float2(nl.x, nl.y), make_float2(nd.x, nd.y), mask);
+          pair(e + 2, make_float2(nl.z, nl.w), make_float2(nd.z, nd.w), mask);
+        }
+      };
+      // Queries past the end already give P = 0 through -LSE*log2e = -inf, so only
+      // the causal boundary and a key row past the end need the per-element test.
+      if (key_ok && q0 + 32 * wg >= i_vis) row(false);
+      else row(true);
       if (t > 0) {  // dV(t-1), dK(t-1) must have read the previous P^T, dS^T
         ok = mbar_wait(&bar->pds_free, static_cast<uint32_t>(t - 1) & 1u, a.status, 0x1305);
-        if (!ok) continue;
+        if (!ok) break;
         tc_fence_after();
       }
       tmem_st16(lane_base + my_pds, pw);
@@ -739,16 +743,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar->sp_free);
       uint32_t dw[32];
+      auto row = [&](bool mask) {
 #pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        const int col = wg * 64 + e;
-        const float2 x = ffma2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sl2v, nl);
-        float2 p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
-        if (col >= cnt) p.x = 0.f;
-        if (col + 1 >= cnt) p.y = 0.f;
-        const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
-        dw[e / 2] = pack_bf16x2(ds.x, ds.y);
-      }
+        for (int e = 0; e < 64; e += 2) {
+          const int col = wg * 64 + e;
+          const float2 x = ffma2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), sl2v, nl);
+          float2 p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+          if (mask) {
+            if (col >= cnt) p.x = 0.f;
+            if (col + 1 >= cnt) p.y = 0.f;
+          }
+          const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
+          dw[e / 2] = pack_bf16x2(ds.x, ds.y);
+        }
+      };
+      if (cnt >= wg * 64 + 64) row(false);  // every key of this warpgroup's half is visible
+      else row(true);
       if (t > 0) {  // dQ(t-1) must have read the previous dS
         ok = mbar_wait(&bar->ds_free, static_cast<uint32_t>(t - 1) & 1u, a.status, 0x2305);
         if (!ok) break;

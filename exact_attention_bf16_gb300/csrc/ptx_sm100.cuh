@@ -219,6 +219,15 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 
+// The same descriptor with its start address moved by `bytes` (a multiple of
+// 16): one 32-bit add on the low word. The 14-bit address field cannot carry
+// into the leading-offset field because shared-memory addresses stay below
+// 256 KB, so a descriptor built once per tile serves all of its k-steps.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+  const uint32_t lo = static_cast<uint32_t>(d) + (bytes >> 4);
+  return (d & 0xFFFFFFFF00000000ull) | lo;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
 // a_mn_major / b_mn_major: operand stored MN-contiguous (else K-contiguous).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn_major, bool b_mn_major) {
