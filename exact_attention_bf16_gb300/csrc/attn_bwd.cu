@@ -633,26 +633,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait_stage = [&](int t) {
         return mbar_wait(&bar->st_full[t % C::NST], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x2210);
       };
-      const uint32_t gb = smem_u32(sdO);
+      // descriptors built once (Q, dO) or once per tile (K, V), advanced per k-step
+      const uint64_t dQd = smem_desc(qb, 16, 1024, SWZ_128B);
+      const uint64_t dOd = smem_desc(smem_u32(sdO), 16, 1024, SWZ_128B);
       auto issue_s = [&](int t) {  // S = Q K^T
-        const uint32_t kb = stage_k(t);
+        const uint64_t dk = smem_desc(stage_k(t), 16, 1024, SWZ_128B);
 #pragma unroll
         for (int kk = 0; kk < DQK / 16; ++kk) {
           const uint32_t off = (kk / 4) * KB * 128 + (kk % 4) * 32;
-          mma_ss(tbase + C::tS, smem_desc(qb + off, 16, 1024, SWZ_128B), smem_desc(kb + off, 16, 1024, SWZ_128B), idS,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(tbase + C::tS, desc_add(dQd, off), desc_add(dk, off), idS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_dp = [&](int t) {  // dP = dO V^T
-        const uint32_t vb = stage_k(t) + C::K_BYTES;
+        const uint64_t dv = smem_desc(stage_k(t) + C::K_BYTES, 16, 1024, SWZ_128B);
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t off = (kk / 4) * KB * 128 + (kk % 4) * 32;
-          const uint64_t bd = smem_desc(vb + off, 16, 1024, SWZ_128B);
+          const uint64_t bd = desc_add(dv, off);
           if constexpr (C::DO_TMEM) {
             mma_ts(tbase + C::tdP, tbase + C::tdO + kk * 8, bd, idS, kk > 0 ? 1u : 0u);
           } else {
-            mma_ss(tbase + C::tdP, smem_desc(gb + off, 16, 1024, SWZ_128B), bd, idS, kk > 0 ? 1u : 0u);
+            mma_ss(tbase + C::tdP, desc_add(dOd, off), bd, idS, kk > 0 ? 1u : 0u);
           }
         }
       };
@@ -678,14 +679,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&bar->ds_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2220);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t kb = stage_k(t);
+        const uint64_t mk = smem_desc(stage_k(t), KB * 128, 1024, SWZ_128B);
+        const uint32_t acc0 = t > 0 ? 1u : 0u;
         // dQ += dS K: A = dS from TMEM (warpgroup w's 64 keys in columns tdS + [32w, 32w+32)),
         // B = K tile read as [d][kv], MN-major
 #pragma unroll
         for (int kk = 0; kk < KB / 16; ++kk) {
           const uint32_t da = tbase + C::tdS + 32 * (kk / 4) + (kk % 4) * 8;
-          mma_ts(tbase + C::tdQ, da, smem_desc(kb + kk * 2048, KB * 128, 1024, SWZ_128B), idQ,
-                 (t > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tbase + C::tdQ, da, desc_add(mk, kk * 2048), idQ, kk > 0 ? 1u : acc0);
         }
         mma_commit(&bar->ds_free);
         mma_commit(&bar->st_empty[t % C::NST]);

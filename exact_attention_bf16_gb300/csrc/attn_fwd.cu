@@ -206,8 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && haveV) ok = mbar_wait(&bar->kv_full[sV], static_cast<uint32_t>(uV / C::NSLOT) & 1u, a.status, 0x211);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t kbase = smem_u32(sKV + sK * C::SLOT);
-        const uint32_t vbase = smem_u32(sKV + sV * C::SLOT);
+        // descriptors built once per tile, advanced per k-step with one add
+        const uint64_t dk = smem_desc(smem_u32(sKV + sK * C::SLOT), 16, 1024, SWZ_128B);
+        const uint64_t dv = smem_desc(smem_u32(sKV + sV * C::SLOT), kChunk, 1024, SWZ_128B);
 #pragma unroll
         for (int i = 0; i < QT; ++i) {
           if (haveV && j - 1 < nkv[i]) {
@@ -215,22 +216,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait(&bar->p_full[i], static_cast<uint32_t>(j - 1) & 1u, a.status, 0x220 + i);
             if (!ok) break;
             tc_fence_after();
+            const uint32_t acc0 = j - 1 > 0 ? 1u : 0u;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t bd = smem_desc(vbase + kk * 2048, kChunk, 1024, SWZ_128B);
-              mma_ts(tbase + tO(i), tbase + tS(i) + kk * 8, bd, idO, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+              mma_ts(tbase + tO(i), tbase + tS(i) + kk * 8, desc_add(dv, kk * 2048), idO, kk > 0 ? 1u : acc0);
             }
             if (j == nkv[i]) mma_commit(&bar->o_full[i]);
           }
           if (j < nkv[i]) {
             // S_i = Q_i K_j^T, both K-major, 16-wide k-steps walking the 128-byte swizzle atoms
-            const uint32_t qbase = smem_u32(sQ + i * C::Q_BYTES);
+            const uint64_t dq = smem_desc(smem_u32(sQ + i * C::Q_BYTES), 16, 1024, SWZ_128B);
 #pragma unroll
             for (int kk = 0; kk < DQK / 16; ++kk) {
               const uint32_t off = (kk / 4) * kChunk + (kk % 4) * 32;
-              const uint64_t ad = smem_desc(qbase + off, 16, 1024, SWZ_128B);
-              const uint64_t bd = smem_desc(kbase + off, 16, 1024, SWZ_128B);
-              mma_ss(tbase + tS(i), ad, bd, idS, kk > 0 ? 1u : 0u);
+              mma_ss(tbase + tS(i), desc_add(dq, off), desc_add(dk, off), idS, kk > 0 ? 1u : 0u);
             }
             mma_commit(&bar->s_full[i]);
           }
