@@ -517,11 +517,15 @@ struct DqCfg {
   static constexpr int DO_BYTES = VCH * MB * 128;
   static constexpr int K_BYTES = QCH * KB * 128;
   static constexpr int V_BYTES = VCH * KB * 128;
-  static constexpr int NST = DQK == 192 ? 1 : 2;
-  static constexpr int STAGE = K_BYTES + V_BYTES;
+  // Separate K and V rings: V(t) is free once dP(t) has read it, K(t) only
+  // after dQ(t), so K gets the extra slot that lets its load start two steps
+  // ahead (one K/V pair per step is more than an SM fetches in one step's time).
+  static constexpr int KST = DQK == 64 ? 4 : DQK == 128 ? 3 : 2;
+  static constexpr int VST = DQK == 64 ? 3 : DQK == 128 ? 2 : 1;
   static constexpr int OFF_DO = Q_BYTES;
-  static constexpr int OFF_ST = OFF_DO + DO_BYTES;
-  static constexpr int OFF_BAR = OFF_ST + NST * STAGE;
+  static constexpr int OFF_K = OFF_DO + DO_BYTES;
+  static constexpr int OFF_V = OFF_K + KST * K_BYTES;
+  static constexpr int OFF_BAR = OFF_V + VST * V_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   // TMEM columns: S | dP | dS | dQ | [dO]
   static constexpr uint32_t tS = 0, tdP = 128, tdS = 256, tdQ = 320, tdO = 320 + DQK;
@@ -532,8 +536,10 @@ struct DqCfg {
 struct DqBars {
   uint64_t q_full;
   uint64_t qd_tmem;
-  uint64_t st_full[2];
-  uint64_t st_empty[2];
+  uint64_t k_full[4];
+  uint64_t k_empty[4];
+  uint64_t v_full[3];
+  uint64_t v_empty[3];
   uint64_t s_full;
   uint64_t sp_free;   // softmax warps hold S(t), dP(t) in registers
   uint64_t ds_free;   // dQ(t) has read dS(t)
@@ -542,6 +548,9 @@ struct DqBars {
   uint64_t mma_done;
   uint32_t tmem_base;
 };
+
+static_assert(sizeof(DqBars) <= 256, "dQ barriers must fit their reserved bytes");
+static_assert(sizeof(DkdvBars) <= 256, "dK/dV barriers must fit their reserved bytes");
 
 __device__ __forceinline__ int key_limit(int row, int nq, int nk, int causal) {
   if (!causal) return nk;
@@ -558,7 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
   uint8_t* sdO = smem + C::OFF_DO;
-  uint8_t* sST = smem + C::OFF_ST;
+  uint8_t* sKr = smem + C::OFF_K;
+  uint8_t* sVr = smem + C::OFF_V;
   DqBars* bar = reinterpret_cast<DqBars*>(smem + C::OFF_BAR);
 
   // (unit, head) slow for L2 sharing of K/V; heaviest (last) query tiles first within a head
@@ -575,9 +585,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
     mbar_init(&bar->qd_tmem, kSoftThreads / 32);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar->st_full[s], 1);
-      mbar_init(&bar->st_empty[s], 1);
+    for (int s = 0; s < C::KST; ++s) {
+      mbar_init(&bar->k_full[s], 1);
+      mbar_init(&bar->k_empty[s], 1);
+    }
+    for (int s = 0; s < C::VST; ++s) {
+      mbar_init(&bar->v_full[s], 1);
+      mbar_init(&bar->v_empty[s], 1);
     }
     mbar_init(&bar->s_full, 1);
     mbar_init(&bar->sp_free, kSoftThreads / 32);
@@ -603,24 +617,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(sQ + c * MB * 128, &tmq, &bar->q_full, c * 64, h, U.q_start + q0, U.b);
       for (int c = 0; c < C::VCH; ++c)
         tma_load_4d(sdO + c * MB * 128, &tmdo, &bar->q_full, c * 64, h, U.q_start + q0, U.b);
-      int issued = 0;
+      int nk_issued = 0, nv_issued = 0;
       bool ok = true;
       for (int t = 0; t < T && ok; ++t) {
-        const int st = t % C::NST;
-        const uint32_t use = static_cast<uint32_t>(t / C::NST);
-        ok = mbar_wait(&bar->st_empty[st], (use & 1u) ^ 1u, a.status, 0x2100 + st);
-        if (!ok) break;
-        uint8_t* dst = sST + st * C::STAGE;
         const int row = U.k_start + t * KB;
-        mbar_arrive_expect_tx(&bar->st_full[st], C::STAGE);
-        for (int c = 0; c < C::QCH; ++c) tma_load_4d(dst + c * KB * 128, &tmk, &bar->st_full[st], c * 64, h, row, U.b);
+        const int ks = t % C::KST, vs = t % C::VST;
+        ok = mbar_wait(&bar->k_empty[ks], (static_cast<uint32_t>(t / C::KST) & 1u) ^ 1u, a.status, 0x2100 + ks);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bar->k_full[ks], C::K_BYTES);
+        for (int c = 0; c < C::QCH; ++c)
+          tma_load_4d(sKr + ks * C::K_BYTES + c * KB * 128, &tmk, &bar->k_full[ks], c * 64, h, row, U.b);
+        ++nk_issued;
+        ok = mbar_wait(&bar->v_empty[vs], (static_cast<uint32_t>(t / C::VST) & 1u) ^ 1u, a.status, 0x2108 + vs);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bar->v_full[vs], C::V_BYTES);
         for (int c = 0; c < C::VCH; ++c)
-          tma_load_4d(dst + C::K_BYTES + c * KB * 128, &tmv, &bar->st_full[st], c * 64, h, row, U.b);
-        ++issued;
+          tma_load_4d(sVr + vs * C::V_BYTES + c * KB * 128, &tmv, &bar->v_full[vs], c * 64, h, row, U.b);
+        ++nv_issued;
       }
-      if (!ok)
-        for (int t = issued - 1; t >= 0 && t >= issued - C::NST; --t)
-          mbar_wait(&bar->st_full[t % C::NST], static_cast<uint32_t>(t / C::NST) & 1u, nullptr, 0);
+      if (!ok) {  // let the copies in flight land before the CTA exits
+        for (int t = nk_issued - 1; t >= 0 && t >= nk_issued - C::KST; --t)
+          mbar_wait(&bar->k_full[t % C::KST], static_cast<uint32_t>(t / C::KST) & 1u, nullptr, 0);
+        for (int t = nv_issued - 1; t >= 0 && t >= nv_issued - C::VST; --t)
+          mbar_wait(&bar->v_full[t % C::VST], static_cast<uint32_t>(t / C::VST) & 1u, nullptr, 0);
+      }
       mbar_wait(&bar->q_full, 0, nullptr, 0);
     }
   } else if (warp == kMmaWarp) {
@@ -629,9 +649,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idQ = idesc_bf16_f32(MB, DQK, false, true);  // B = K tile, MN-major
       bool ok = mbar_wait(&bar->qd_tmem, 0, a.status, 0x2200);
       const uint32_t qb = smem_u32(sQ);
-      auto stage_k = [&](int t) { return smem_u32(sST + (t % C::NST) * C::STAGE); };
-      auto wait_stage = [&](int t) {
-        return mbar_wait(&bar->st_full[t % C::NST], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x2210);
+      auto stage_k = [&](int t) { return smem_u32(sKr + (t % C::KST) * C::K_BYTES); };
+      auto stage_v = [&](int t) { return smem_u32(sVr + (t % C::VST) * C::V_BYTES); };
+      auto wait_stage = [&](int t) {  // K(t) and V(t) have landed
+        return mbar_wait(&bar->k_full[t % C::KST], static_cast<uint32_t>(t / C::KST) & 1u, a.status, 0x2210) &&
+               mbar_wait(&bar->v_full[t % C::VST], static_cast<uint32_t>(t / C::VST) & 1u, a.status, 0x2211);
       };
       // descriptors built once (Q, dO) or once per tile (K, V), advanced per k-step
       const uint64_t dQd = smem_desc(qb, 16, 1024, SWZ_128B);
@@ -645,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto issue_dp = [&](int t) {  // dP = dO V^T
-        const uint64_t dv = smem_desc(stage_k(t) + C::K_BYTES, 16, 1024, SWZ_128B);
+        const uint64_t dv = smem_desc(stage_v(t), 16, 1024, SWZ_128B);
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk) {
           const uint32_t off = (kk / 4) * KB * 128 + (kk % 4) * 32;
@@ -665,16 +687,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_s(0);
           issue_dp(0);
           mma_commit(&bar->s_full);
+          mma_commit(&bar->v_empty[0]);
         }
       }
       for (int t = 0; t < T && ok; ++t) {
-        if (C::NST > 1 && t + 1 < T) {  // next S, dP as soon as the softmax warps hold this tile's
+        if (t + 1 < T) {  // next S, dP as soon as the softmax warps hold this tile's
           ok = mbar_wait(&bar->sp_free, static_cast<uint32_t>(t) & 1u, a.status, 0x2215) && wait_stage(t + 1);
           if (!ok) break;
           tc_fence_after();
           issue_s(t + 1);
           issue_dp(t + 1);
           mma_commit(&bar->s_full);
+          mma_commit(&bar->v_empty[(t + 1) % C::VST]);
         }
         ok = mbar_wait(&bar->ds_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2220);
         if (!ok) break;
@@ -689,15 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tbase + C::tdQ, da, desc_add(mk, kk * 2048), idQ, kk > 0 ? 1u : acc0);
         }
         mma_commit(&bar->ds_free);
-        mma_commit(&bar->st_empty[t % C::NST]);
-        if (C::NST == 1 && t + 1 < T) {  // one stage: the next K/V tile arrives only after this dQ has read K(t)
-          ok = wait_stage(t + 1);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(t + 1);
-          issue_dp(t + 1);
-          mma_commit(&bar->s_full);
-        }
+        mma_commit(&bar->k_empty[t % C::KST]);
       }
       mma_commit(&bar->acc_full);
       mma_commit(&bar->mma_done);
