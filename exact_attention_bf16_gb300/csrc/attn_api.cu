@@ -220,7 +220,7 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
 }
 
 
-int bwd_dkdv_rows(int) { return 64; }  // query rows per step of the dK/dV kernel
+int bwd_dkdv_rows(int d_qk) { return d_qk == 128 ? 128 : 64; }  // query rows per step of the dK/dV kernel
 
 size_t bwd_workspace_bytes(const attn_bwd_params* p, bool varlen) {
   const attn_fwd_params& f = p->fwd;

@@ -159,7 +159,7 @@ struct DkdvCfg {
   static constexpr int V_BYTES = VCH * KB * 128;
   static constexpr int QT_BYTES = QCH * QB * 128;   // one query tile of Q
   static constexpr int DOT_BYTES = VCH * QB * 128;  // one query tile of dO
-  static constexpr int NST = 3;
+  static constexpr int NST = DQK == 192 ? 3 : 4;  // query-tile stages (as many as shared memory holds)
   static constexpr int STAGE = QT_BYTES + DOT_BYTES;
   static constexpr int OFF_V = K_BYTES;
   static constexpr int OFF_ST = OFF_V + V_BYTES;
@@ -173,8 +173,8 @@ struct DkdvCfg {
 struct DkdvBars {
   uint64_t kv_full;
   uint64_t kv_tmem;
-  uint64_t st_full[3];
-  uint64_t st_empty[3];
+  uint64_t st_full[4];
+  uint64_t st_empty[4];
   uint64_t s_full;
   uint64_t sp_free;   // softmax warps hold S^T(t), dP^T(t) in registers
   uint64_t pds_free;  // dV(t), dK(t) have read P^T(t), dS^T(t)
@@ -257,9 +257,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < T && ok; ++t) {
       const int st = t % C::NST;
       const uint32_t use = static_cast<uint32_t>(t / C::NST);
+      const int tile = (m_begin + t) * QB;
+      // fetch the vectors first, so their latency overlaps the wait for the slot
+      float nl[QB / 32], nd[QB / 32];
+#pragma unroll
+      for (int u = 0; u < QB / 32; ++u) {
+        const int r = static_cast<int>(lane) + 32 * u;
+        nl[u] = -INFINITY;  // rows past the end: P = 0
+        nd[u] = 0.f;
+        if (tile + r < U.nq) {
+          const int64_t idx = U.b * a.lse_sb + h * a.lse_sh + U.q_start + tile + r;
+          const float l = a.lse[idx];
+          nl[u] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;  // P = 2^(S * scale * log2e + nl)
+          nd[u] = -a.dsum[idx];
+        }
+      }
       ok = mbar_wait(&bar->st_empty[st], (use & 1u) ^ 1u, a.status, 0x1100 + st);
       if (!ok) break;
-      const int tile = (m_begin + t) * QB;
       if (lane == 0) {
         uint8_t* dst = sST + st * C::STAGE;
         const int row = U.q_start + tile;
@@ -270,16 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float* vec = sVec + st * 2 * QB;
 #pragma unroll
-      for (int r = static_cast<int>(lane); r < QB; r += 32) {
-        float nl = -INFINITY, nd = 0.f;  // rows past the end: P = 0
-        if (tile + r < U.nq) {
-          const int64_t idx = U.b * a.lse_sb + h * a.lse_sh + U.q_start + tile + r;
-          const float l = a.lse[idx];
-          nl = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;  // P = 2^(S * scale * log2e + nl)
-          nd = -a.dsum[idx];
-        }
-        vec[r] = nl;
-        vec[QB + r] = nd;
+      for (int u = 0; u < QB / 32; ++u) {
+        vec[lane + 32 * u] = nl[u];
+        vec[QB + lane + 32 * u] = nd[u];
       }
       mbar_arrive(&bar->st_full[st]);
       ++issued;
@@ -492,6 +499,377 @@ __global__ void __launch_bounds__(kThreads, 1)
                        : 0u;
         if (store) store_row_bf16(dst + c * 32, w);
       }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tbase, 512);
+}
+
+// ===========================================================================
+// dK / dV kernel for d_qk = d_v = 128: 128 query rows per step
+// ===========================================================================
+// With 64-row steps the S^T and dP^T MMAs are only N = 64 wide, and the one
+// thread that issues MMAs cannot keep the tensor core busy with them. Here a
+// step is 128 queries, so every MMA is N = 128. TMEM then holds two 128-column
+// regions besides the dV and dK accumulators (512 columns in all):
+//   S^T(t) -> R(t) and dP^T(t) -> R'(t), the other region;
+//   the softmax warps write P^T(t) and dS^T(t) over S^T(t) in R(t);
+//   S^T(t+1) -> R'(t) once they have copied dP^T(t) out (sp_free);
+//   dP^T(t+1) -> R(t), issued after dV(t) and dK(t), which read R(t): MMAs run
+//   in issue order, so the overwrite comes after those reads.
+// The softmax work of a step is split: P from S^T (phase A) needs only S^T and
+// the LSE vector, so it runs while the tensor core computes dV, dK of the
+// previous step and dP^T of this one; dS from dP^T (phase B) follows.
+struct DkdvWCfg {
+  static constexpr int QB = 128, D = 128;
+  static constexpr uint32_t tR0 = 0, tR1 = 128, tdV = 256, tdK = 384;
+  static constexpr int TILE = QB * D * 2;            // one 128 x 128 bf16 tile: 32 KB
+  static constexpr int NQ = 3, NG = 2, NVEC = 2;     // Q, dO and vector ring slots
+  static constexpr int OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE;
+  static constexpr int OFF_G = OFF_Q + NQ * TILE;
+  static constexpr int OFF_VEC = OFF_G + NG * TILE;  // [NVEC][2][QB] floats: -LSE*log2e, -D
+  static constexpr int OFF_BAR = OFF_VEC + NVEC * 2 * QB * 4;
+  static constexpr int SMEM = OFF_BAR + 256;         // the base is 1024-byte aligned (checked)
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct DkdvWBars {
+  uint64_t kv_full;
+  uint64_t q_full[3], q_empty[3];
+  uint64_t g_full[2], g_empty[2];
+  uint64_t v_full[2], v_empty[2];
+  uint64_t s_full;    // S^T(t) in TMEM
+  uint64_t dp_full;   // dP^T(t) in TMEM
+  uint64_t sp_free;   // softmax warps hold dP^T(t) in registers
+  uint64_t ds_full;   // P^T(t), dS^T(t) written
+  uint64_t acc_full;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+};
+static_assert(sizeof(DkdvWBars) <= 256, "dK/dV barriers must fit their reserved bytes");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv_wide_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo, const BwdArgs a) {
+  using C = DkdvWCfg;
+  constexpr int QB = C::QB;
+  extern __shared__ __align__(1024) uint8_t smem_w[];
+  if ((smem_u32(smem_w) & 1023u) != 0u) {  // the 128-byte-swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) record_error(a.status, DEV_BAD_CONFIG, 0x1400);
+    return;
+  }
+  uint8_t* sK = smem_w + C::OFF_K;
+  uint8_t* sV = smem_w + C::OFF_V;
+  uint8_t* sQ = smem_w + C::OFF_Q;
+  uint8_t* sG = smem_w + C::OFF_G;
+  float* sVec = reinterpret_cast<float*>(smem_w + C::OFF_VEC);
+  DkdvWBars* bar = reinterpret_cast<DkdvWBars*>(smem_w + C::OFF_BAR);
+
+  // same work order as dkdv_kernel: (unit, head) slow, key tile 0 (the heaviest under causal) first
+  const int bh = static_cast<int>(blockIdx.x) / a.n_kblk;
+  const int n = static_cast<int>(blockIdx.x) % a.n_kblk;
+  const int h = bh % a.heads;
+  const Unit U = unit_bounds(a, bh / a.heads);
+  const int k0 = n * KB;
+  if (k0 >= U.nk) return;
+  int m_begin = 0;
+  if (a.causal) {
+    const int i_min = k0 - (U.nk - U.nq);  // first query row that sees key k0
+    m_begin = i_min > 0 ? i_min / QB : 0;
+  }
+  const int m_end = ceil_div(U.nq, QB);
+  const int T = m_end > m_begin ? m_end - m_begin : 0;
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    mbar_init(&bar->kv_full, 1);
+    for (int s = 0; s < C::NQ; ++s) {
+      mbar_init(&bar->q_full[s], 1);
+      mbar_init(&bar->q_empty[s], 1);
+    }
+    for (int s = 0; s < C::NG; ++s) {
+      mbar_init(&bar->g_full[s], 1);
+      mbar_init(&bar->g_empty[s], 1);
+    }
+    for (int s = 0; s < C::NVEC; ++s) {
+      mbar_init(&bar->v_full[s], 32);                 // every loader lane
+      mbar_init(&bar->v_empty[s], kSoftThreads / 32);  // every softmax warp
+    }
+    mbar_init(&bar->s_full, 1);
+    mbar_init(&bar->dp_full, 1);
+    mbar_init(&bar->sp_free, kSoftThreads / 32);
+    mbar_init(&bar->ds_full, kSoftThreads / 32);
+    mbar_init(&bar->acc_full, 1);
+    mbar_init(&bar->mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bar->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bar->tmem_base;
+  auto region = [](int t) { return (t & 1) ? C::tR1 : C::tR0; };        // R(t): S^T(t), then P^T/dS^T(t)
+  auto other = [](int t) { return (t & 1) ? C::tR0 : C::tR1; };         // R'(t): dP^T(t)
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar->kv_full, 2 * C::TILE);
+      for (int c = 0; c < 2; ++c) tma_load_4d(sK + c * KB * 128, &tmk, &bar->kv_full, c * 64, h, U.k_start + k0, U.b);
+      for (int c = 0; c < 2; ++c) tma_load_4d(sV + c * KB * 128, &tmv, &bar->kv_full, c * 64, h, U.k_start + k0, U.b);
+    }
+    // Lane 0 streams the Q and dO tiles; every lane writes four of the tile's
+    // 128 (-LSE*log2e, -D) pairs into the vector ring and arrives on its barrier.
+    int nq_issued = 0, ng_issued = 0;
+    bool ok = true;
+    for (int t = 0; t < T && ok; ++t) {
+      const int tile = (m_begin + t) * QB;
+      const int row = U.q_start + tile;
+      float nl[QB / 32], nd[QB / 32];  // fetched first, so their latency overlaps the waits below
+#pragma unroll
+      for (int u = 0; u < QB / 32; ++u) {
+        const int r = static_cast<int>(lane) + 32 * u;
+        nl[u] = -INFINITY;  // rows past the end: P = 0
+        nd[u] = 0.f;
+        if (tile + r < U.nq) {
+          const int64_t idx = U.b * a.lse_sb + h * a.lse_sh + U.q_start + tile + r;
+          const float l = a.lse[idx];
+          nl[u] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;  // P = 2^(S * scale * log2e + nl)
+          nd[u] = -a.dsum[idx];
+        }
+      }
+      const int qs = t % C::NQ, gs = t % C::NG, vs = t % C::NVEC;
+      ok = mbar_wait(&bar->q_empty[qs], (static_cast<uint32_t>(t / C::NQ) & 1u) ^ 1u, a.status, 0x1400 + qs);
+      if (!ok) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar->q_full[qs], C::TILE);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sQ + qs * C::TILE + c * QB * 128, &tmq, &bar->q_full[qs], c * 64, h, row, U.b);
+      }
+      ++nq_issued;
+      ok = mbar_wait(&bar->g_empty[gs], (static_cast<uint32_t>(t / C::NG) & 1u) ^ 1u, a.status, 0x1408 + gs);
+      if (!ok) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar->g_full[gs], C::TILE);
+        for (int c = 0; c < 2; ++c)
+          tma_load_4d(sG + gs * C::TILE + c * QB * 128, &tmdo, &bar->g_full[gs], c * 64, h, row, U.b);
+      }
+      ++ng_issued;
+      ok = mbar_wait(&bar->v_empty[vs], (static_cast<uint32_t>(t / C::NVEC) & 1u) ^ 1u, a.status, 0x1410 + vs);
+      if (!ok) break;
+      float* vec = sVec + vs * 2 * QB;
+#pragma unroll
+      for (int u = 0; u < QB / 32; ++u) {
+        vec[lane + 32 * u] = nl[u];
+        vec[QB + lane + 32 * u] = nd[u];
+      }
+      mbar_arrive(&bar->v_full[vs]);
+    }
+    if (lane == 0) {
+      if (!ok) {  // let the copies in flight land before the CTA exits
+        for (int t = nq_issued - 1; t >= 0 && t >= nq_issued - C::NQ; --t)
+          mbar_wait(&bar->q_full[t % C::NQ], static_cast<uint32_t>(t / C::NQ) & 1u, nullptr, 0);
+        for (int t = ng_issued - 1; t >= 0 && t >= ng_issued - C::NG; --t)
+          mbar_wait(&bar->g_full[t % C::NG], static_cast<uint32_t>(t / C::NG) & 1u, nullptr, 0);
+      }
+      mbar_wait(&bar->kv_full, 0, nullptr, 0);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(KB, QB, false, false);  // S^T, dP^T: B = Q / dO tile, K-major
+      constexpr uint32_t idA = idesc_bf16_f32(KB, 128, false, true);  // dV, dK: B = dO / Q tile, MN-major
+      const uint64_t dKd = smem_desc(smem_u32(sK), 16, 1024, SWZ_128B);
+      const uint64_t dVd = smem_desc(smem_u32(sV), 16, 1024, SWZ_128B);
+      auto q_tile = [&](int t) { return smem_u32(sQ + (t % C::NQ) * C::TILE); };
+      auto g_tile = [&](int t) { return smem_u32(sG + (t % C::NG) * C::TILE); };
+      auto issue_s = [&](int t) {  // S^T(t) = K Q^T -> R(t)
+        const uint64_t bq = smem_desc(q_tile(t), 16, 1024, SWZ_128B);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk / 4) * KB * 128 + (kk % 4) * 32;
+          mma_ss(tbase + region(t), desc_add(dKd, off), desc_add(bq, off), idS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_dp = [&](int t) {  // dP^T(t) = V dO^T -> R'(t)
+        const uint64_t bg = smem_desc(g_tile(t), 16, 1024, SWZ_128B);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk / 4) * KB * 128 + (kk % 4) * 32;
+          mma_ss(tbase + other(t), desc_add(dVd, off), desc_add(bg, off), idS, kk > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(&bar->kv_full, 0, a.status, 0x1420);
+      if (ok && T > 0) {
+        ok = mbar_wait(&bar->q_full[0], 0, a.status, 0x1421);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+          mma_commit(&bar->s_full);
+          ok = mbar_wait(&bar->g_full[0], 0, a.status, 0x1422);
+        }
+        if (ok) {
+          tc_fence_after();
+          issue_dp(0);
+          mma_commit(&bar->dp_full);
+        }
+      }
+      for (int t = 0; t < T && ok; ++t) {
+        if (t + 1 < T) {  // S^T(t+1) into R'(t) once the softmax warps hold dP^T(t)
+          ok = mbar_wait(&bar->sp_free, static_cast<uint32_t>(t) & 1u, a.status, 0x1425) &&
+               mbar_wait(&bar->q_full[(t + 1) % C::NQ], static_cast<uint32_t>((t + 1) / C::NQ) & 1u, a.status, 0x1426);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(t + 1);
+          mma_commit(&bar->s_full);
+        }
+        ok = mbar_wait(&bar->ds_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1428);
+        if (!ok) break;
+        tc_fence_after();
+        // dV += P^T dO and dK += dS^T Q, A from R(t): the 16 queries of k-step kk
+        // belong to warpgroup kk/4, half (kk%4)/2 of its 64, whose 32 columns
+        // hold P^T in the first 16 and dS^T in the last 16
+        const uint64_t mg = smem_desc(g_tile(t), QB * 128, 1024, SWZ_128B);
+        const uint64_t mq = smem_desc(q_tile(t), QB * 128, 1024, SWZ_128B);
+        const uint32_t acc0 = t > 0 ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < QB / 16; ++kk) {
+          const uint32_t pa = tbase + region(t) + 64 * (kk / 4) + 32 * ((kk % 4) / 2) + 8 * (kk % 2);
+          mma_ts(tbase + C::tdV, pa, desc_add(mg, kk * 2048), idA, kk > 0 ? 1u : acc0);
+        }
+        mma_commit(&bar->g_empty[t % C::NG]);
+#pragma unroll
+        for (int kk = 0; kk < QB / 16; ++kk) {
+          const uint32_t da = tbase + region(t) + 64 * (kk / 4) + 32 * ((kk % 4) / 2) + 16 + 8 * (kk % 2);
+          mma_ts(tbase + C::tdK, da, desc_add(mq, kk * 2048), idA, kk > 0 ? 1u : acc0);
+        }
+        mma_commit(&bar->q_empty[t % C::NQ]);
+        if (t + 1 < T) {  // dP^T(t+1) into R(t), after the reads above in issue order
+          ok = mbar_wait(&bar->g_full[(t + 1) % C::NG], static_cast<uint32_t>((t + 1) / C::NG) & 1u, a.status, 0x142a);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(t + 1);
+          mma_commit(&bar->dp_full);
+        }
+      }
+      mma_commit(&bar->acc_full);
+      mma_commit(&bar->mma_done);
+      mbar_wait(&bar->mma_done, 0, a.status, 0x14ff);
+    }
+  } else {
+    // ================= softmax gradient: one key row per thread ============
+    const int wg = static_cast<int>(warp) / 4;           // which 64 of the 128 query columns
+    const uint32_t quarter = warp & 3u;
+    const int j = static_cast<int>(quarter * 32 + lane);  // key row within the tile
+    const int kj = k0 + j;
+    const uint32_t lane_base = tbase + ((quarter * 32u) << 16);
+    const int i_vis = a.causal ? kj - (U.nk - U.nq) : -0x40000000;  // queries i >= i_vis see key kj
+    const bool key_ok = kj < U.nk;
+    const float2 sl2v = make_float2(a.scale_log2, a.scale_log2);
+    bool ok = true;
+    for (int t = 0; t < T && ok; ++t) {
+      const int q0 = (m_begin + t) * QB + 64 * wg;  // this warpgroup's first query
+      const uint32_t my = lane_base + region(t) + 64 * wg;
+      // ---- phase A: P from S^T(t), written over S^T(t) as bf16 P^T
+      ok = mbar_wait(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1430) &&
+           mbar_wait(&bar->v_full[t % C::NVEC], static_cast<uint32_t>(t / C::NVEC) & 1u, a.status, 0x1431);
+      if (!ok) break;
+      tc_fence_after();
+      const float* vL = sVec + (t % C::NVEC) * 2 * QB + 64 * wg;
+      const float* vD = vL + QB;
+      const bool full = key_ok && q0 >= i_vis;  // every query of this warpgroup sees this key
+      float p[64];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sv[32], pw[16];
+        tmem_ld32(my + 32 * hh, sv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 nl = *reinterpret_cast<const float4*>(vL + 32 * hh + e);
+          const float2 x0 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2v,
+                                  make_float2(nl.x, nl.y));
+          const float2 x1 = ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), sl2v,
+                                  make_float2(nl.z, nl.w));
+          float* pp = p + 32 * hh + e;
+          pp[0] = ex2_mufu(x0.x);
+          pp[1] = ex2_mufu(x0.y);
+          pp[2] = ex2_mufu(x1.x);
+          pp[3] = ex2_mufu(x1.y);
+          if (!full) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (!(key_ok && q0 + 32 * hh + e + u >= i_vis)) pp[u] = 0.f;
+          }
+          pw[e / 2] = pack_bf16x2(pp[0], pp[1]);
+          pw[e / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
+        }
+        tmem_st16(my + 32 * hh, pw);
+      }
+      // ---- phase B: dS = P (dP - D) from dP^T(t), written next to P^T
+      ok = mbar_wait(&bar->dp_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1432);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dp[64];
+      tmem_ld32(lane_base + other(t) + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+      tmem_ld32(lane_base + other(t) + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar->sp_free);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t dw[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 nd = *reinterpret_cast<const float4*>(vD + 32 * hh + e);
+          const int c = 32 * hh + e;
+          const float2 d0 = fmul2(make_float2(p[c], p[c + 1]),
+                                  fadd2(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
+                                        make_float2(nd.x, nd.y)));
+          const float2 d1 = fmul2(make_float2(p[c + 2], p[c + 3]),
+                                  fadd2(make_float2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])),
+                                        make_float2(nd.z, nd.w)));
+          dw[e / 2] = pack_bf16x2(d0.x, d0.y);
+          dw[e / 2 + 1] = pack_bf16x2(d1.x, d1.y);
+        }
+        tmem_st16(my + 32 * hh + 16, dw);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bar->ds_full);
+        mbar_arrive(&bar->v_empty[t % C::NVEC]);
+      }
+    }
+    // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
+    if (ok && T > 0) {
+      ok = mbar_wait(&bar->acc_full, 0, a.status, 0x1440);
+      tc_fence_after();
+    }
+    const bool store = key_ok;
+    __nv_bfloat16* dst = wg == 0 ? static_cast<__nv_bfloat16*>(a.dv) + U.b * a.dv_sb +
+                                       static_cast<int64_t>(U.k_start + kj) * a.dv_sn + h * a.dv_sh
+                                 : static_cast<__nv_bfloat16*>(a.dk) + U.b * a.dk_sb +
+                                       static_cast<int64_t>(U.k_start + kj) * a.dk_sn + h * a.dk_sh;
+    const uint32_t acc = wg == 0 ? C::tdV : C::tdK;
+    const float mul = wg == 0 ? 1.f : a.scale;
+#pragma unroll
+    for (int c = 0; c < C::D / 32; ++c) {
+      uint32_t v[32], w[16];
+      if (T > 0) {
+        tmem_ld32(lane_base + acc + c * 32, v);
+        tmem_wait_ld();
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        w[e] = T > 0 ? pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul) : 0u;
+      if (store) store_row_bf16(dst + c * 32, w);
     }
   }
 
@@ -852,6 +1230,21 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   return cudaGetLastError();
 }
 
+cudaError_t launch_dkdv_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = set_smem(dkdv_wide_kernel, DkdvWCfg::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int64_t grid = static_cast<int64_t>(a.n_kblk) * a.num_units * a.heads;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  dkdv_wide_kernel<<<static_cast<unsigned>(grid), kThreads, DkdvWCfg::SMEM, stream>>>(tq, tk, tv, tdo, a);
+  return cudaGetLastError();
+}
+
 template <int DQK, int DV>
 cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                         const BwdArgs& a, cudaStream_t stream) {
@@ -886,7 +1279,7 @@ cudaError_t launch_bwd_preprocess(int d_v, const BwdArgs& a, cudaStream_t stream
 cudaError_t launch_bwd_dkdv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
   if (d_qk == 64 && d_v == 64) return bwd::launch_dkdv_t<64, 64>(tq, tk, tv, tdo, a, stream);
-  if (d_qk == 128 && d_v == 128) return bwd::launch_dkdv_t<128, 128>(tq, tk, tv, tdo, a, stream);
+  if (d_qk == 128 && d_v == 128) return bwd::launch_dkdv_wide(tq, tk, tv, tdo, a, stream);
   if (d_qk == 192 && d_v == 128) return bwd::launch_dkdv_t<192, 128>(tq, tk, tv, tdo, a, stream);
   return cudaErrorInvalidValue;
 }
