@@ -40,9 +40,9 @@ WORKLOAD = dict(batch=4, heads=16, seqlen=8192, d_qk=128, d_v=128)
 # Measured on the non-causal B=2, H=16, N=8192 case (profiles/*_B2H16N8192.md) and
 # scaled x2 to the benchmark's B=4 launch (traffic grows with the (batch, head) units).
 KERNEL_TRAFFIC_NCU = {
-    "dkdv_kernel": {"source_sha": "5be9d6bc954f25e1", "bytes_per_launch": 2 * (270.770944e6 + 104.943616e6)},
-    "dq_kernel": {"source_sha": "5be9d6bc954f25e1", "bytes_per_launch": 2 * (271.210752e6 + 52.315392e6)},
-    "attn_fwd_kernel": {"source_sha": "d0dfaa2f80c54e34", "bytes_per_launch": 2 * (201.885952e6 + 46.822400e6)},
+    "dkdv_wide_kernel": {"source_sha": "942a281a9abce53a", "bytes_per_launch": 2 * (271.245312e6 + 104.830208e6)},
+    "dq_kernel": {"source_sha": "942a281a9abce53a", "bytes_per_launch": 2 * (270.870272e6 + 52.336640e6)},
+    "attn_fwd_kernel": {"source_sha": "7e74a3038e576900", "bytes_per_launch": 2 * (201.447424e6 + 46.002688e6)},
 }
 
 
@@ -283,8 +283,8 @@ def run_gpu(args):
         barrier()
     elapsed_ms = ev0.elapsed_time(ev1)
     # per-kernel durations: forward (one launch per pass); backward phases from the library's events
-    per_kernel = {"attn_fwd_kernel": [], "bwd_preprocess_kernel": [], "dkdv_kernel": [], "dq_kernel": []}
-    kernel_flops = {"attn_fwd_kernel": [], "bwd_preprocess_kernel": [], "dkdv_kernel": [], "dq_kernel": []}
+    per_kernel = {"attn_fwd_kernel": [], "bwd_preprocess_kernel": [], "dkdv_wide_kernel": [], "dq_kernel": []}
+    kernel_flops = {"attn_fwd_kernel": [], "bwd_preprocess_kernel": [], "dkdv_wide_kernel": [], "dq_kernel": []}
     for s in range(args.steps):
         for key in flops:
             a, b = evs[s][key]
@@ -294,12 +294,12 @@ def run_gpu(args):
             b0 = evs[s][("bwd", c)][0]
             per_kernel["attn_fwd_kernel"].append(evs[s][("fwd", c)][0].elapsed_time(evs[s][("fwd", c)][1]))
             per_kernel["bwd_preprocess_kernel"].append(b0.elapsed_time(ph[0]))
-            per_kernel["dkdv_kernel"].append(ph[0].elapsed_time(ph[1]))
+            per_kernel["dkdv_wide_kernel"].append(ph[0].elapsed_time(ph[1]))
             per_kernel["dq_kernel"].append(ph[1].elapsed_time(ph[2]))
             pairs = w.batch * w.heads * (N * N / 2.0 if c else float(N) * N)
             kernel_flops["attn_fwd_kernel"].append(2 * pairs * (w.d_qk + w.d_v))
             kernel_flops["bwd_preprocess_kernel"].append(0.0)
-            kernel_flops["dkdv_kernel"].append(2 * pairs * (2 * w.d_qk + 2 * w.d_v))  # S^T, dP^T, dV, dK
+            kernel_flops["dkdv_wide_kernel"].append(2 * pairs * (2 * w.d_qk + 2 * w.d_v))  # S^T, dP^T, dV, dK
             kernel_flops["dq_kernel"].append(2 * pairs * (2 * w.d_qk + w.d_v))        # S, dP, dQ
     ea.attn_get_device_status()
     elapsed_ms = reduce_max(elapsed_ms, dev)
@@ -363,7 +363,7 @@ def run_gpu(args):
     rec = KERNEL_TRAFFIC_NCU.get(dom, {})
     traffic = rec.get("bytes_per_launch") if rec.get("source_sha") == src_sha else None
     step_ms = sum(totals.values()) / args.steps
-    roofline = {"kernel": f"{dom}<128,128> (mean over non-causal and causal launches)", "bound": "tensor",
+    roofline = {"kernel": f"{dom} d=128 (mean over non-causal and causal launches)", "bound": "tensor",
                 "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
                 "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long step)",
                 "frac_of_nominal_2250": achieved / NOMINAL_PEAK_TFLOPS, "traffic": traffic,
