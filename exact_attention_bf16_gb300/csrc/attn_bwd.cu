@@ -731,20 +731,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         // dV += P^T dO and dK += dS^T Q, A from R(t): the 16 queries of k-step kk
-        // belong to warpgroup kk/4, half (kk%4)/2 of its 64, whose 32 columns
-        // hold P^T in the first 16 and dS^T in the last 16
+        // belong to warpgroup kk/4, whose 64 columns hold P^T (bf16 pairs) in the
+        // first 32 and dS^T in the last 32
         const uint64_t mg = smem_desc(g_tile(t), QB * 128, 1024, SWZ_128B);
         const uint64_t mq = smem_desc(q_tile(t), QB * 128, 1024, SWZ_128B);
         const uint32_t acc0 = t > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < QB / 16; ++kk) {
-          const uint32_t pa = tbase + region(t) + 64 * (kk / 4) + 32 * ((kk % 4) / 2) + 8 * (kk % 2);
+          const uint32_t pa = tbase + region(t) + 64 * (kk / 4) + 8 * (kk % 4);
           mma_ts(tbase + C::tdV, pa, desc_add(mg, kk * 2048), idA, kk > 0 ? 1u : acc0);
         }
         mma_commit(&bar->g_empty[t % C::NG]);
 #pragma unroll
         for (int kk = 0; kk < QB / 16; ++kk) {
-          const uint32_t da = tbase + region(t) + 64 * (kk / 4) + 32 * ((kk % 4) / 2) + 16 + 8 * (kk % 2);
+          const uint32_t da = tbase + region(t) + 64 * (kk / 4) + 32 + 8 * (kk % 4);
           mma_ts(tbase + C::tdK, da, desc_add(mq, kk * 2048), idA, kk > 0 ? 1u : acc0);
         }
         mma_commit(&bar->q_empty[t % C::NQ]);
@@ -761,83 +761,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&bar->mma_done, 0, a.status, 0x14ff);
     }
   } else {
-    // ================= softmax gradient: one key row per thread ============
-    const int wg = static_cast<int>(warp) / 4;           // which 64 of the 128 query columns
+    // ================= softmax gradient ====================================
+    // Warp w reads its lane quarter in the 16x256b fragment layout: per 16-lane
+    // group lg, thread (g, c) = (lane / 4, lane % 4) holds key rows g and g + 8
+    // at query columns 8r + 2c and 8r + 2c + 1 (r = 0..7) of its warpgroup's 64.
+    // A thread so needs the LSE and D of only 16 queries per step (8 float2
+    // loads each), and each adjacent pair packs into the bf16x2 column 4r + c
+    // that the 16x128b store writes.
+    const int wg = static_cast<int>(warp) / 4;  // which 64 of the 128 query columns
     const uint32_t quarter = warp & 3u;
-    const int j = static_cast<int>(quarter * 32 + lane);  // key row within the tile
-    const int kj = k0 + j;
-    const uint32_t lane_base = tbase + ((quarter * 32u) << 16);
-    const int i_vis = a.causal ? kj - (U.nk - U.nq) : -0x40000000;  // queries i >= i_vis see key kj
-    const bool key_ok = kj < U.nk;
+    const int g = static_cast<int>(lane >> 2), c = static_cast<int>(lane & 3u);
+    int vis[2][2];    // [lane group][row g or g + 8]: queries i >= vis see the key
+    bool kok[2][2];
+#pragma unroll
+    for (int lg = 0; lg < 2; ++lg)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int kj = k0 + static_cast<int>(quarter) * 32 + 16 * lg + 8 * hh + g;
+        vis[lg][hh] = a.causal ? kj - (U.nk - U.nq) : -0x40000000;
+        kok[lg][hh] = kj < U.nk;
+      }
+    const bool all_keys = kok[0][0] && kok[0][1] && kok[1][0] && kok[1][1];
+    const int vis_max = max(max(vis[0][0], vis[0][1]), max(vis[1][0], vis[1][1]));
     const float2 sl2v = make_float2(a.scale_log2, a.scale_log2);
+    auto lanes = [&](int lg) { return tbase + ((quarter * 32u + 16u * static_cast<uint32_t>(lg)) << 16); };
     bool ok = true;
     for (int t = 0; t < T && ok; ++t) {
       const int q0 = (m_begin + t) * QB + 64 * wg;  // this warpgroup's first query
-      const uint32_t my = lane_base + region(t) + 64 * wg;
+      const uint32_t col = region(t) + 64 * wg;
       // ---- phase A: P from S^T(t), written over S^T(t) as bf16 P^T
       ok = mbar_wait(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1430) &&
            mbar_wait(&bar->v_full[t % C::NVEC], static_cast<uint32_t>(t / C::NVEC) & 1u, a.status, 0x1431);
       if (!ok) break;
       tc_fence_after();
-      const float* vL = sVec + (t % C::NVEC) * 2 * QB + 64 * wg;
+      const float* vL = sVec + (t % C::NVEC) * 2 * QB + 64 * wg + 2 * c;
       const float* vD = vL + QB;
-      const bool full = key_ok && q0 >= i_vis;  // every query of this warpgroup sees this key
-      float p[64];
+      const bool full = all_keys && q0 >= vis_max;  // every (key, query) cell of this thread is visible
+      float p[2][32];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+      for (int lg = 0; lg < 2; ++lg) {
         uint32_t sv[32], pw[16];
-        tmem_ld32(my + 32 * hh, sv);
+        tmem_ld16x256b_x8(lanes(lg) + col, sv);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 nl = *reinterpret_cast<const float4*>(vL + 32 * hh + e);
-          const float2 x0 = ffma2(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2v,
-                                  make_float2(nl.x, nl.y));
-          const float2 x1 = ffma2(make_float2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), sl2v,
-                                  make_float2(nl.z, nl.w));
-          float* pp = p + 32 * hh + e;
+        for (int r = 0; r < 8; ++r) {
+          const float2 nl = *reinterpret_cast<const float2*>(vL + 8 * r);
+          const float2 x0 = ffma2(make_float2(__uint_as_float(sv[4 * r]), __uint_as_float(sv[4 * r + 1])), sl2v, nl);
+          const float2 x1 = ffma2(make_float2(__uint_as_float(sv[4 * r + 2]), __uint_as_float(sv[4 * r + 3])), sl2v, nl);
+          float* pp = &p[lg][4 * r];
           pp[0] = ex2_mufu(x0.x);
           pp[1] = ex2_mufu(x0.y);
           pp[2] = ex2_mufu(x1.x);
           pp[3] = ex2_mufu(x1.y);
           if (!full) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (!(key_ok && q0 + 32 * hh + e + u >= i_vis)) pp[u] = 0.f;
+            for (int u = 0; u < 4; ++u) {
+              const int qi = q0 + 8 * r + 2 * c + (u & 1);
+              if (!(kok[lg][u >> 1] && qi >= vis[lg][u >> 1])) pp[u] = 0.f;
+            }
           }
-          pw[e / 2] = pack_bf16x2(pp[0], pp[1]);
-          pw[e / 2 + 1] = pack_bf16x2(pp[2], pp[3]);
+          pw[2 * r] = pack_bf16x2(pp[0], pp[1]);
+          pw[2 * r + 1] = pack_bf16x2(pp[2], pp[3]);
         }
-        tmem_st16(my + 32 * hh, pw);
+        tmem_st16x128b_x8(lanes(lg) + col, pw);
       }
       // ---- phase B: dS = P (dP - D) from dP^T(t), written next to P^T
       ok = mbar_wait(&bar->dp_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1432);
       if (!ok) break;
       tc_fence_after();
-      uint32_t dp[64];
-      tmem_ld32(lane_base + other(t) + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
-      tmem_ld32(lane_base + other(t) + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+      uint32_t dp[2][32];
+      tmem_ld16x256b_x8(lanes(0) + other(t) + 64 * wg, dp[0]);
+      tmem_ld16x256b_x8(lanes(1) + other(t) + 64 * wg, dp[1]);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar->sp_free);
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
+      for (int lg = 0; lg < 2; ++lg) {
         uint32_t dw[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 nd = *reinterpret_cast<const float4*>(vD + 32 * hh + e);
-          const int c = 32 * hh + e;
-          const float2 d0 = fmul2(make_float2(p[c], p[c + 1]),
-                                  fadd2(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
-                                        make_float2(nd.x, nd.y)));
-          const float2 d1 = fmul2(make_float2(p[c + 2], p[c + 3]),
-                                  fadd2(make_float2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])),
-                                        make_float2(nd.z, nd.w)));
-          dw[e / 2] = pack_bf16x2(d0.x, d0.y);
-          dw[e / 2 + 1] = pack_bf16x2(d1.x, d1.y);
+        for (int r = 0; r < 8; ++r) {
+          const float2 nd = *reinterpret_cast<const float2*>(vD + 8 * r);
+          const float2 d0 = fmul2(make_float2(p[lg][4 * r], p[lg][4 * r + 1]),
+                                  fadd2(make_float2(__uint_as_float(dp[lg][4 * r]), __uint_as_float(dp[lg][4 * r + 1])), nd));
+          const float2 d1 = fmul2(make_float2(p[lg][4 * r + 2], p[lg][4 * r + 3]),
+                                  fadd2(make_float2(__uint_as_float(dp[lg][4 * r + 2]), __uint_as_float(dp[lg][4 * r + 3])), nd));
+          dw[2 * r] = pack_bf16x2(d0.x, d0.y);
+          dw[2 * r + 1] = pack_bf16x2(d1.x, d1.y);
         }
-        tmem_st16(my + 32 * hh + 16, dw);
+        tmem_st16x128b_x8(lanes(lg) + col + 32, dw);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -847,12 +859,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bar->v_empty[t % C::NVEC]);
       }
     }
-    // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
+    // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK (one key row per thread)
     if (ok && T > 0) {
       ok = mbar_wait(&bar->acc_full, 0, a.status, 0x1440);
       tc_fence_after();
     }
-    const bool store = key_ok;
+    const int kj = k0 + static_cast<int>(quarter * 32 + lane);
+    const uint32_t lane_base = tbase + ((quarter * 32u) << 16);
+    const bool store = kj < U.nk;
     __nv_bfloat16* dst = wg == 0 ? static_cast<__nv_bfloat16*>(a.dv) + U.b * a.dv_sb +
                                        static_cast<int64_t>(U.k_start + kj) * a.dv_sn + h * a.dv_sh
                                  : static_cast<__nv_bfloat16*>(a.dk) + U.b * a.dk_sb +
