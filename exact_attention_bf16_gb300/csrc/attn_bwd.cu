@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = a.scale_log2;
     const uint32_t my_cols = C::tS + 32 * wg;     // this warpgroup's S^T columns
     const uint32_t my_pds = C::tPdS + 32 * wg;    // its P^T (16) and dS^T (16) columns
-    bool ok = mbar_wait(&bar->kv_full, 0, a.status, 0x1301);
+    bool ok = mbar_wait_warp(&bar->kv_full, 0, a.status, 0x1301);
     // K (warpgroup 0) and V (warpgroup 1) rows into TMEM as MMA A operands, where they fit
     if (ok) {
       if (wg == 0) {
@@ -410,9 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float2 sl2v = make_float2(sl2, sl2);
     for (int t = 0; t < T && ok; ++t) {
       const int q0 = (m_begin + t) * QB;
-      ok = mbar_wait(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1300);
+      ok = mbar_wait_warp(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1300);
       // this tile's (-LSE*log2e, -D) vectors, written by the loader lanes
-      if (ok) ok = mbar_wait(&bar->st_full[t % C::NST], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x1302);
+      if (ok) ok = mbar_wait_warp(&bar->st_full[t % C::NST], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x1302);
       if (!ok) break;
       tc_fence_after();
       const float* vL = sVec + (t % C::NST) * 2 * QB + 32 * wg;
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (key_ok && q0 + 32 * wg >= i_vis) row(false);
       else row(true);
       if (t > 0) {  // dV(t-1), dK(t-1) must have read the previous P^T, dS^T
-        ok = mbar_wait(&bar->pds_free, static_cast<uint32_t>(t - 1) & 1u, a.status, 0x1305);
+        ok = mbar_wait_warp(&bar->pds_free, static_cast<uint32_t>(t - 1) & 1u, a.status, 0x1305);
         if (!ok) break;
         tc_fence_after();
       }
@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
     if (ok && T > 0) {
-      ok = mbar_wait(&bar->acc_full, 0, a.status, 0x1310);
+      ok = mbar_wait_warp(&bar->acc_full, 0, a.status, 0x1310);
       tc_fence_after();
     }
     const bool store = key_ok;
@@ -790,8 +790,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = (m_begin + t) * QB + 64 * wg;  // this warpgroup's first query
       const uint32_t col = region(t) + 64 * wg;
       // ---- phase A: P from S^T(t), written over S^T(t) as bf16 P^T
-      ok = mbar_wait(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1430) &&
-           mbar_wait(&bar->v_full[t % C::NVEC], static_cast<uint32_t>(t / C::NVEC) & 1u, a.status, 0x1431);
+      ok = mbar_wait_warp(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1430) &&
+           mbar_wait_warp(&bar->v_full[t % C::NVEC], static_cast<uint32_t>(t / C::NVEC) & 1u, a.status, 0x1431);
       if (!ok) break;
       tc_fence_after();
       const float* vL = sVec + (t % C::NVEC) * 2 * QB + 64 * wg + 2 * c;
@@ -826,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16x128b_x8(lanes(lg) + col, pw);
       }
       // ---- phase B: dS = P (dP - D) from dP^T(t), written next to P^T
-      ok = mbar_wait(&bar->dp_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1432);
+      ok = mbar_wait_warp(&bar->dp_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1432);
       if (!ok) break;
       tc_fence_after();
       uint32_t dp[2][32];
@@ -861,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK (one key row per thread)
     if (ok && T > 0) {
-      ok = mbar_wait(&bar->acc_full, 0, a.status, 0x1440);
+      ok = mbar_wait_warp(&bar->acc_full, 0, a.status, 0x1440);
       tc_fence_after();
     }
     const int kj = k0 + static_cast<int>(quarter * 32 + lane);
@@ -1126,7 +1126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       dsum = a.dsum[U.b * a.lse_sb + h * a.lse_sh + U.q_start + i];
     }
     const float sl2 = a.scale_log2;
-    bool ok = mbar_wait(&bar->q_full, 0, a.status, 0x2301);
+    bool ok = mbar_wait_warp(&bar->q_full, 0, a.status, 0x2301);
     // dO rows into TMEM as the A operand of dP, where it fits
     if (ok && wg == 1) {
       if constexpr (C::DO_TMEM) tile_row_to_tmem(sdO, C::VCH, r, lane_base + C::tdO);
@@ -1137,7 +1137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(&bar->qd_tmem);
     const float2 sl2v = make_float2(sl2, sl2), nl = make_float2(-lse2, -lse2), nd = make_float2(-dsum, -dsum);
     for (int t = 0; t < T && ok; ++t) {
-      ok = mbar_wait(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2300);
+      ok = mbar_wait_warp(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2300);
       if (!ok) break;
       tc_fence_after();
       const int cnt = lim - t * KB;  // visible keys of this row in tile t
@@ -1169,7 +1169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (cnt >= wg * 64 + 64) row(false);  // every key of this warpgroup's half is visible
       else row(true);
       if (t > 0) {  // dQ(t-1) must have read the previous dS
-        ok = mbar_wait(&bar->ds_free, static_cast<uint32_t>(t - 1) & 1u, a.status, 0x2305);
+        ok = mbar_wait_warp(&bar->ds_free, static_cast<uint32_t>(t - 1) & 1u, a.status, 0x2305);
         if (!ok) break;
         tc_fence_after();
       }
@@ -1180,7 +1180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bar->ds_full);
     }
     if (ok && T > 0) {
-      ok = mbar_wait(&bar->acc_full, 0, a.status, 0x2310);
+      ok = mbar_wait_warp(&bar->acc_full, 0, a.status, 0x2310);
       tc_fence_after();
     }
     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + U.b * a.dq_sb +

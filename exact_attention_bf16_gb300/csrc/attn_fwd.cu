@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n_rescale = 0, n_opp = 0;
     bool ok = true;
     for (int j = 0; j < nkv[i]; ++j) {
-      ok = mbar_wait(&bar->s_full[i], static_cast<uint32_t>(j) & 1u, a.status, 0x300 + i);
+      ok = mbar_wait_warp(&bar->s_full[i], static_cast<uint32_t>(j) & 1u, a.status, 0x300 + i);
       if (!ok) break;
       tc_fence_after();
       uint32_t s[BN];
@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue: O = acc / l (exact normalisation), LSE = ln2 * (m + log2 l)
     if (ok && nkv[i] > 0) {
-      ok = mbar_wait(&bar->o_full[i], 0, a.status, 0x310 + i);
+      ok = mbar_wait_warp(&bar->o_full[i], 0, a.status, 0x310 + i);
       tc_fence_after();
     }
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;

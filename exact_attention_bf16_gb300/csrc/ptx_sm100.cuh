@@ -87,6 +87,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// mbar_wait for code that all 32 lanes of a warp run together and that issues
+// warp-collective instructions (tcgen05.ld/st, votes) afterwards: if any lane's
+// wait failed, every lane sees false, so the warp leaves its loop as one.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status, uint32_t where) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, where));
+}
+
 // ---------------------------------------------------------------------------
 // Proxy fences
 // ---------------------------------------------------------------------------
