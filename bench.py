@@ -312,37 +312,70 @@ def run_gpu(args):
             "ms": med, "tflops": flops[(direction, causal)] / (med * 1e-3) / 1e12}
 
     # ---- end to end through the public API with host buffers ------------------
+    # Every step copies its inputs (Q, K, V, dO) from pinned host memory to the
+    # device, runs the forward and the backward for both masks through the
+    # public API, and copies every output (O, LSE, dQ, dK, dV of both masks)
+    # back to pinned host memory. Steps are pipelined over two device buffer
+    # sets on three streams (copy in, compute, copy out), so one step's copies
+    # overlap its neighbours' compute; all copies of all timed steps lie inside
+    # the timed region.
     host_in = {n: t[n].cpu().pin_memory() for n in ("q", "k", "v", "do")}
-    host_out = {c: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o[c], lse[c], *grads[c])]
-                for c in (False, True)}
+    nbuf = 2
+    dev_in = [{n: torch.empty_like(t[n]) for n in host_in} for _ in range(nbuf)]
+    dev_out = [{c: [torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev),
+                    torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)] for c in (False, True)}
+               for _ in range(nbuf)]
+    host_out = [{c: [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in dev_out[i][c]] for c in (False, True)}
+                for i in range(nbuf)]
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
-    d2h = sum(x.numel() * x.element_size() for c in (False, True) for x in host_out[c])
-    dev_in = {n: torch.empty_like(t[n]) for n in host_in}
+    d2h = sum(x.numel() * x.element_size() for c in (False, True) for x in host_out[0][c])
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_cmp = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]
 
-    def e2e_step():
-        for n in host_in:
-            dev_in[n].copy_(host_in[n], non_blocking=True)
+    def e2e_step(kstep):
+        i = kstep % nbuf
+        s_in.wait_event(ev_cmp[i])  # buffer i's inputs were last read by step kstep - 2
+        with torch.cuda.stream(s_in):
+            for n in host_in:
+                dev_in[i][n].copy_(host_in[n], non_blocking=True)
+            ev_in[i].record(s_in)
+        stream.wait_event(ev_in[i])
+        stream.wait_event(ev_out[i])  # buffer i's outputs of step kstep - 2 are back on the host
+        qi, ki, vi, doi = (dev_in[i][n] for n in ("q", "k", "v", "do"))
         for causal in (False, True):
-            oo, ll = ea.attn_fwd(dev_in["q"], dev_in["k"], dev_in["v"], causal=causal, softmax_scale=w.scale,
-                                 out=o[causal], lse=lse[causal])
-            g = ea.attn_bwd(dev_in["q"], dev_in["k"], dev_in["v"], oo, ll, dev_in["do"], causal=causal,
-                            softmax_scale=w.scale, dq=grads[causal][0], dk=grads[causal][1], dv=grads[causal][2])
-            for dst, src in zip(host_out[causal], (oo, ll, *g)):
-                dst.copy_(src, non_blocking=True)
+            oo, ll, dq_, dk_, dv_ = dev_out[i][causal]
+            ea.attn_fwd(qi, ki, vi, causal=causal, softmax_scale=w.scale, out=oo, lse=ll, stream=stream)
+            ea.attn_bwd(qi, ki, vi, oo, ll, doi, causal=causal, softmax_scale=w.scale, dq=dq_, dk=dk_, dv=dv_,
+                        stream=stream)
+        ev_cmp[i].record(stream)
+        s_out.wait_event(ev_cmp[i])
+        with torch.cuda.stream(s_out):
+            for causal in (False, True):
+                for dst, src in zip(host_out[i][causal], dev_out[i][causal]):
+                    dst.copy_(src, non_blocking=True)
+            ev_out[i].record(s_out)
 
-    for _ in range(max(1, args.warmup // 2)):
-        e2e_step()
+    for kstep in range(max(2, args.warmup)):
+        e2e_step(kstep)
     torch.cuda.synchronize(dev)
     barrier()
-    e_steps = max(2, args.steps // 2)
+    e_steps = max(4, args.steps // 2)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
+    s_in.wait_event(a)
+    s_out.wait_event(a)
+    for kstep in range(e_steps):
+        e2e_step(kstep)
+    for i in range(nbuf):
+        stream.wait_event(ev_out[i])
     b.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = reduce_max(a.elapsed_time(b), dev)
     e2e_value = world * total_flops * e_steps / (e2e_ms * 1e-3) / 1e12
+    # the last step's results, as read back, must match the device-resident run
+    assert torch.equal(host_out[(e_steps - 1) % nbuf][True][1], lse[True].cpu()), "end-to-end LSE differs"
 
     if rank != 0:
         if world > 1:
