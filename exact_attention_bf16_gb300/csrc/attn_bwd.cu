@@ -797,6 +797,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* vL = sVec + (t % C::NVEC) * 2 * QB + 64 * wg + 2 * c;
       const float* vD = vL + QB;
       const bool full = all_keys && q0 >= vis_max;  // every (key, query) cell of this thread is visible
+      float2 nlv[8];  // -LSE*log2e of this thread's 16 queries (the same for both lane groups)
+#pragma unroll
+      for (int r = 0; r < 8; ++r) nlv[r] = *reinterpret_cast<const float2*>(vL + 8 * r);
       float p[2][32];
 #pragma unroll
       for (int lg = 0; lg < 2; ++lg) {
@@ -805,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
-          const float2 nl = *reinterpret_cast<const float2*>(vL + 8 * r);
+          const float2 nl = nlv[r];
           const float2 x0 = ffma2(make_float2(__uint_as_float(sv[4 * r]), __uint_as_float(sv[4 * r + 1])), sl2v, nl);
           const float2 x1 = ffma2(make_float2(__uint_as_float(sv[4 * r + 2]), __uint_as_float(sv[4 * r + 3])), sl2v, nl);
           float* pp = &p[lg][4 * r];
@@ -836,12 +839,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar->sp_free);
+      float2 ndv[8];  // -D of the same 16 queries
+#pragma unroll
+      for (int r = 0; r < 8; ++r) ndv[r] = *reinterpret_cast<const float2*>(vD + 8 * r);
 #pragma unroll
       for (int lg = 0; lg < 2; ++lg) {
         uint32_t dw[16];
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
-          const float2 nd = *reinterpret_cast<const float2*>(vD + 8 * r);
+          const float2 nd = ndv[r];
           const float2 d0 = fmul2(make_float2(p[lg][4 * r], p[lg][4 * r + 1]),
                                   fadd2(make_float2(__uint_as_float(dp[lg][4 * r]), __uint_as_float(dp[lg][4 * r + 1])), nd));
           const float2 d1 = fmul2(make_float2(p[lg][4 * r + 2], p[lg][4 * r + 3]),
