@@ -81,31 +81,44 @@ __device__ __forceinline__ Unit unit_bounds(const BwdArgs& a, int unit) {
 }
 
 // ===========================================================================
-// Preprocess: D = rowsum(dO * O), one warp per (row, head).
+// Preprocess: D = rowsum(dO * O). HBM-bound: DV / 8 lanes share a row, each
+// loading 16 bytes of O and of dO per access (rows and head slices start on
+// 16-byte boundaries, as the TMA tensor maps already require).
 // ===========================================================================
 template <int DV>
 __global__ void preprocess_kernel(const BwdArgs a) {
+  constexpr int LPR = DV / 8;    // lanes per row
+  constexpr int RPW = 32 / LPR;  // rows per warp
   const int64_t rows = static_cast<int64_t>(a.batch) * a.seqlen_q * a.heads;
   const int64_t warp0 = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int lane = threadIdx.x & 31;
-  for (int64_t r = warp0; r < rows; r += nwarps) {
-    const int h = static_cast<int>(r % a.heads);
-    const int64_t bi = r / a.heads;
-    const int i = static_cast<int>(bi % a.seqlen_q);
-    const int b = static_cast<int>(bi / a.seqlen_q);
-    const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(a.o) + b * a.o_sb + i * a.o_sn + h * a.o_sh;
-    const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(a.dout) + b * a.do_sb + i * a.do_sn + h * a.do_sh;
+  const int sub = lane / LPR, l = lane % LPR;
+  for (int64_t r0 = warp0 * RPW; r0 < rows; r0 += nwarps * RPW) {
+    const int64_t r = r0 + sub;
     float acc = 0.f;
-    for (int c = lane * 2; c < DV; c += 64) {
-      const __nv_bfloat162 ov = *reinterpret_cast<const __nv_bfloat162*>(o + c);
-      const __nv_bfloat162 gv = *reinterpret_cast<const __nv_bfloat162*>(g + c);
-      acc = fmaf(__bfloat162float(ov.x), __bfloat162float(gv.x), acc);
-      acc = fmaf(__bfloat162float(ov.y), __bfloat162float(gv.y), acc);
+    int h = 0, i = 0, b = 0;
+    if (r < rows) {
+      h = static_cast<int>(r % a.heads);
+      const int64_t bi = r / a.heads;
+      i = static_cast<int>(bi % a.seqlen_q);
+      b = static_cast<int>(bi / a.seqlen_q);
+      const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(a.o) + b * a.o_sb + i * a.o_sn + h * a.o_sh;
+      const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(a.dout) + b * a.do_sb + i * a.do_sn + h * a.do_sh;
+      const uint4 ov = *reinterpret_cast<const uint4*>(o + 8 * l);
+      const uint4 gv = *reinterpret_cast<const uint4*>(g + 8 * l);
+      const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 of = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[e]));
+        const float2 gf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+        acc = fmaf(of.x, gf.x, acc);
+        acc = fmaf(of.y, gf.y, acc);
+      }
     }
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) a.dsum[b * a.lse_sb + h * a.lse_sh + i] = acc;
+    for (int s = LPR / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (r < rows && l == 0) a.dsum[b * a.lse_sb + h * a.lse_sh + i] = acc;
   }
 }
 
@@ -1289,7 +1302,9 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 cudaError_t launch_bwd_preprocess(int d_v, const BwdArgs& a, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(a.batch) * a.seqlen_q * a.heads;
   if (rows == 0) return cudaSuccess;
-  const int64_t blocks = (rows * 32 + 255) / 256 < 16384 ? (rows * 32 + 255) / 256 : 16384;
+  const int64_t per_block = 8 * (d_v == 64 ? 4 : 2);  // 8 warps, each 32 / (d_v / 8) rows per pass
+  const int64_t want = (rows + per_block - 1) / per_block;
+  const int64_t blocks = want < 16384 ? want : 16384;
   if (d_v == 64) bwd::preprocess_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
   else if (d_v == 128) bwd::preprocess_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
   else return cudaErrorInvalidValue;
