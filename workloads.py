@@ -144,6 +144,22 @@ def make_varlen(w: Workload, device="cpu", with_do: bool = True):
     return out
 
 
+def make_varlen_qk(q_lengths, k_lengths, heads: int, d_qk: int, d_v: int, seed: int, device="cpu"):
+    """Packed varlen inputs whose query and key lengths differ per sequence:
+    dict(q [total_q, H, d_qk], k, v [total_k, H, d], do [total_q, H, d_v],
+    cu_q, cu_k), i.i.d. N(0,1) rounded to bf16 from one seeded generator."""
+    assert len(q_lengths) == len(k_lengths)
+    tq, tk = sum(q_lengths), sum(k_lengths)
+    g = torch.Generator(device=device).manual_seed(seed)
+    f32 = dict(generator=g, device=device, dtype=torch.float32)
+    q = torch.randn((tq, heads, d_qk), **f32).to(torch.bfloat16)
+    k = torch.randn((tk, heads, d_qk), **f32).to(torch.bfloat16)
+    v = torch.randn((tk, heads, d_v), **f32).to(torch.bfloat16)
+    do = torch.randn((tq, heads, d_v), **f32).to(torch.bfloat16)
+    return {"q": q, "k": k, "v": v, "do": do, "cu_q": cu_seqlens_of(q_lengths).to(device),
+            "cu_k": cu_seqlens_of(k_lengths).to(device)}
+
+
 def sample_pairs(batch: int, heads: int, n: int, seed: int = 1234):
     """A seeded subset of (batch, head) units for spot-checking large workloads."""
     g = torch.Generator().manual_seed(seed)
