@@ -169,3 +169,11 @@ def test_workspace_errors(ea):
     assert lib.attn_bwd(ctypes.byref(p), ctypes.c_void_p(ws.data_ptr()), need - 16, None) == _abi.ATTN_ERR_WORKSPACE
     assert lib.attn_bwd(ctypes.byref(p), ctypes.c_void_p(ws.data_ptr()), need, None) == _abi.ATTN_OK
     torch.cuda.synchronize()
+
+
+def test_outlier_variant_sampled(ea):
+    # 1% of key rows scaled x8: rows whose attention concentrates on a few keys
+    w = workloads.dense_d128(4096, causal=False, outlier=True)
+    t = workloads.make_dense(w, device="cuda")
+    dq, dk, dv = gpu_fwd_bwd(ea, t, w)
+    check_pairs(t, w, dq, dk, dv, workloads.sample_pairs(w.batch, w.heads, 2, seed=4096))
