@@ -40,24 +40,6 @@ constexpr int kSoftThreads = 256;
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Stores 32 bf16 values (16 packed words) into row `row` of a K-major,
-// 128-byte-swizzled tile whose 64-column chunks are `chunk_bytes` apart,
-// starting at column col0 (a multiple of 32).
-__device__ __forceinline__ void st_swizzled_row32(uint8_t* tile, int chunk_bytes, int row, int col0,
-                                                  const uint32_t (&w)[16]) {
-  uint8_t* base = tile + (col0 / 64) * chunk_bytes + row * 128;
-  const int u0 = (col0 % 64) / 8;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int pu = (u0 + u) ^ (row & 7);
-    *reinterpret_cast<uint4*>(base + pu * 16) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-  }
-}
-
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&w)[16]) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -1297,7 +1279,6 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 }
 
 }  // namespace bwd
-
 
 cudaError_t launch_bwd_preprocess(int d_v, const BwdArgs& a, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(a.batch) * a.seqlen_q * a.heads;
