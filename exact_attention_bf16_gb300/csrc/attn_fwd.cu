@@ -304,8 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < BN / 2; ++c) {
         const float2 x = ffma2(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sl2v, negmu);
         float2 p;
-        if (EMU_PERIOD > 0 && ((2 * c) % EMU_PERIOD) == EMU_PERIOD - 2) {
-          p = make_float2(ex2_mufu(x.x), ex2_emu(x.y));
+        if constexpr (EMU_PERIOD > 0) {
+          if (((2 * c) % EMU_PERIOD) == EMU_PERIOD - 2) {
+            p = make_float2(ex2_mufu(x.x), ex2_emu(x.y));
+          } else {
+            p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+          }
         } else {
           p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
         }
