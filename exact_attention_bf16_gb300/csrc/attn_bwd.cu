@@ -1232,12 +1232,9 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           const BwdArgs& a, cudaStream_t stream) {
   using C = DkdvCfg<DQK, DV>;
   auto kern = dkdv_kernel<DQK, DV>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(kern, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static PerDeviceOnce once;
+  cudaError_t e = once.run([&] { return set_smem(kern, C::SMEM); });
+  if (e != cudaSuccess) return e;
   const int64_t grid = static_cast<int64_t>(a.n_kblk) * a.num_units * a.heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
@@ -1247,12 +1244,9 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 
 cudaError_t launch_dkdv_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(dkdv_wide_kernel, DkdvWCfg::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static PerDeviceOnce once;
+  cudaError_t e = once.run([] { return set_smem(dkdv_wide_kernel, DkdvWCfg::SMEM); });
+  if (e != cudaSuccess) return e;
   const int64_t grid = static_cast<int64_t>(a.n_kblk) * a.num_units * a.heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
@@ -1265,12 +1259,9 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
                         const BwdArgs& a, cudaStream_t stream) {
   using C = DqCfg<DQK, DV>;
   auto kern = dq_kernel<DQK, DV>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = set_smem(kern, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static PerDeviceOnce once;
+  cudaError_t e = once.run([&] { return set_smem(kern, C::SMEM); });
+  if (e != cudaSuccess) return e;
   const int64_t grid = static_cast<int64_t>(a.n_qblk) * a.num_units * a.heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;

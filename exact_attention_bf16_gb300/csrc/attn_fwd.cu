@@ -413,17 +413,17 @@ cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
                      cudaStream_t stream) {
   using C = Cfg<DQK, DV>;
   auto kern = attn_fwd_kernel<DQK, DV, EMU>;
-  static bool attr_done = false;  // benign race: the attribute calls are idempotent
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
+  static PerDeviceOnce once;
+  cudaError_t e = once.run([&]() -> cudaError_t {
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (r != cudaSuccess) return r;
     cudaFuncAttributes fa{};
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
+    r = cudaFuncGetAttributes(&fa, kern);
+    if (r != cudaSuccess) return r;
     // The setmaxnreg split must fit in the registers the CTA is launched with.
-    if (fa.numRegs * kThreads < C::REG_BUDGET) return cudaErrorInvalidConfiguration;
-    attr_done = true;
-  }
+    return fa.numRegs * kThreads < C::REG_BUDGET ? cudaErrorInvalidConfiguration : cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   const int64_t grid = static_cast<int64_t>(a.n_mblk) * a.num_units * a.heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;

@@ -3,9 +3,30 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstdint>
 
 namespace gb300 {
+
+// One-time launch configuration of a kernel (its shared-memory limit and
+// checks), done once per device: cudaFuncSetAttribute applies to the current
+// device, so every GPU a process launches on must see it. Devices 0..63 are
+// remembered; on others the configuration simply runs again.
+struct PerDeviceOnce {
+  std::atomic<uint64_t> done{0};
+  template <typename F>
+  cudaError_t run(F&& configure) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+    e = configure();
+    if (e != cudaSuccess) return e;
+    if (bit != 0) done.fetch_or(bit, std::memory_order_release);
+    return cudaSuccess;
+  }
+};
 
 // Forward kernel arguments (passed by value; tensor maps go separately as
 // __grid_constant__ parameters).
