@@ -40,9 +40,9 @@ WORKLOAD = dict(batch=4, heads=16, seqlen=8192, d_qk=128, d_v=128)
 # Measured on the non-causal B=2, H=16, N=8192 case (profiles/*_B2H16N8192.md) and
 # scaled x2 to the benchmark's B=4 launch (traffic grows with the (batch, head) units).
 KERNEL_TRAFFIC_NCU = {
-    "dkdv_wide_kernel": {"source_sha": "942a281a9abce53a", "bytes_per_launch": 2 * (271.245312e6 + 104.830208e6)},
-    "dq_kernel": {"source_sha": "942a281a9abce53a", "bytes_per_launch": 2 * (270.870272e6 + 52.336640e6)},
-    "attn_fwd_kernel": {"source_sha": "7e74a3038e576900", "bytes_per_launch": 2 * (201.447424e6 + 46.002688e6)},
+    "dkdv_wide_kernel": {"source_sha": "c84cb542be2f329c", "bytes_per_launch": 2 * (270.917376e6 + 104.7552e6)},
+    "dq_kernel": {"source_sha": "c84cb542be2f329c", "bytes_per_launch": 2 * (270.679808e6 + 52.036608e6)},
+    "attn_fwd_kernel": {"source_sha": "7b89da9206a28ab1", "bytes_per_launch": 2 * (201.413632e6 + 45.540608e6)},
 }
 
 
