@@ -121,7 +121,10 @@ typedef struct attn_fwd_params {
  * (read-only here), shapes, scale and mask; dout is the incoming gradient dO
  * (bf16, same layout rules as o); dq, dk, dv (bf16) are written. With
  * deterministic != 0 the dQ reduction runs in a fixed order and repeated calls
- * on identical inputs give bitwise-identical dq/dk/dv on the same device. */
+ * on identical inputs give bitwise-identical dq/dk/dv on the same device. This
+ * implementation reduces dQ inside one query-stationary CTA per tile (no
+ * atomics, no cross-CTA reduction), so deterministic == 0 reproduces bitwise
+ * too; the flag is accepted for interface compatibility. */
 typedef struct attn_bwd_params {
   attn_fwd_params fwd;
   const void* dout;
