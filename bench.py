@@ -316,7 +316,7 @@ def run_gpu(args):
     # device, runs the forward and the backward for both masks through the
     # public API, and copies every output (O, LSE, dQ, dK, dV of both masks)
     # back to pinned host memory. Steps are pipelined over two device buffer
-    # sets on three streams (copy in, compute, copy out), so one step's copies
+    # sets, with copies on their own streams (in and out), so one step's copies
     # overlap its neighbours' compute; all copies of all timed steps lie inside
     # the timed region.
     host_in = {n: t[n].cpu().pin_memory() for n in ("q", "k", "v", "do")}
@@ -329,20 +329,32 @@ def run_gpu(args):
                 for i in range(nbuf)]
     h2d = sum(x.numel() * x.element_size() for x in host_in.values())
     d2h = sum(x.numel() * x.element_size() for c in (False, True) for x in host_out[0][c])
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+    # Several copy streams per direction, each moving ~32 MB pieces, keep more than
+    # one copy engine busy on the host link.
+    n_cs = 4
+    s_in = [torch.cuda.Stream(dev) for _ in range(n_cs)]
+    s_out = [torch.cuda.Stream(dev) for _ in range(n_cs)]
+    ev_in = [[torch.cuda.Event() for _ in range(n_cs)] for _ in range(nbuf)]
     ev_cmp = [torch.cuda.Event() for _ in range(nbuf)]
-    ev_out = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_out = [[torch.cuda.Event() for _ in range(n_cs)] for _ in range(nbuf)]
+    piece = 32 << 20
+
+    def pieces(dst, src):
+        d, sv = dst.view(-1), src.view(-1)
+        step = max(1, piece // dst.element_size())
+        return [(d[a:a + step], sv[a:a + step]) for a in range(0, d.numel(), step)]
 
     def e2e_step(kstep):
         i = kstep % nbuf
-        s_in.wait_event(ev_cmp[i])  # buffer i's inputs were last read by step kstep - 2
-        with torch.cuda.stream(s_in):
-            for n in host_in:
-                dev_in[i][n].copy_(host_in[n], non_blocking=True)
-            ev_in[i].record(s_in)
-        stream.wait_event(ev_in[i])
-        stream.wait_event(ev_out[i])  # buffer i's outputs of step kstep - 2 are back on the host
+        jobs = [pc for n in host_in for pc in pieces(dev_in[i][n], host_in[n])]
+        for c in range(n_cs):
+            s_in[c].wait_event(ev_cmp[i])  # buffer i's inputs were last read by step kstep - 2
+            with torch.cuda.stream(s_in[c]):
+                for dst, src in jobs[c::n_cs]:
+                    dst.copy_(src, non_blocking=True)
+                ev_in[i][c].record(s_in[c])
+            stream.wait_event(ev_in[i][c])
+            stream.wait_event(ev_out[i][c])  # buffer i's outputs of step kstep - 2 are back on the host
         qi, ki, vi, doi = (dev_in[i][n] for n in ("q", "k", "v", "do"))
         for causal in (False, True):
             oo, ll, dq_, dk_, dv_ = dev_out[i][causal]
@@ -350,12 +362,14 @@ def run_gpu(args):
             ea.attn_bwd(qi, ki, vi, oo, ll, doi, causal=causal, softmax_scale=w.scale, dq=dq_, dk=dk_, dv=dv_,
                         stream=stream)
         ev_cmp[i].record(stream)
-        s_out.wait_event(ev_cmp[i])
-        with torch.cuda.stream(s_out):
-            for causal in (False, True):
-                for dst, src in zip(host_out[i][causal], dev_out[i][causal]):
+        jobs = [pc for causal in (False, True) for dst, src in zip(host_out[i][causal], dev_out[i][causal])
+                for pc in pieces(dst, src)]
+        for c in range(n_cs):
+            s_out[c].wait_event(ev_cmp[i])
+            with torch.cuda.stream(s_out[c]):
+                for dst, src in jobs[c::n_cs]:
                     dst.copy_(src, non_blocking=True)
-            ev_out[i].record(s_out)
+                ev_out[i][c].record(s_out[c])
 
     for kstep in range(max(2, args.warmup)):
         e2e_step(kstep)
@@ -364,12 +378,14 @@ def run_gpu(args):
     e_steps = max(4, args.steps // 2)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    s_in.wait_event(a)
-    s_out.wait_event(a)
+    for c in range(n_cs):
+        s_in[c].wait_event(a)
+        s_out[c].wait_event(a)
     for kstep in range(e_steps):
         e2e_step(kstep)
     for i in range(nbuf):
-        stream.wait_event(ev_out[i])
+        for c in range(n_cs):
+            stream.wait_event(ev_out[i][c])
     b.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = reduce_max(a.elapsed_time(b), dev)
