@@ -53,13 +53,38 @@ def visible_limit(i, nq: int, nk: int, causal: bool):
     return np.clip(i + (nk - nq) + 1, 0, nk).astype(np.int64)
 
 
-def _logits(q, k, softmax_scale, rows, nq, nk, causal):
-    """a_ij = scale * q_i . k_j for visible j, -inf elsewhere (rows = row indices)."""
+def _logits(q, k, softmax_scale, rows, nq, nk, causal, visible=None):
+    """a_ij = scale * q_i . k_j for visible j, -inf elsewhere (rows = row indices).
+    ``visible`` (optional bool [Nq, Nk]) hides further keys (AND with the causal mask)."""
     a = softmax_scale * (q[rows] @ k.T)
     lim = visible_limit(rows, nq, nk, causal)
     cols = np.arange(nk)
     a[cols[None, :] >= lim[:, None]] = -np.inf
+    if visible is not None:
+        a[~np.asarray(visible, dtype=bool)[rows]] = -np.inf
     return a
+
+
+def block_sparse_visible(nq: int, nk: int, kv_count, kv_index, q_block: int = 256, k_block: int = 128):
+    """Key visibility of a block-sparse mask, written out element by element.
+
+    The mask lists, for each block of ``q_block`` query rows, the blocks of
+    ``k_block`` keys it attends to: query block b sees key blocks
+    kv_index[b, 0 .. kv_count[b]-1] (FlexAttention / block-sparse variants
+    built on FA4: wittx "FlashAttention-4", section Python写GPU内核). Entries
+    outside [0, ceil(nk / k_block)) list nothing. Returns bool [nq, nk].
+    """
+    kv_count = np.asarray(kv_count).reshape(-1)
+    kv_index = np.asarray(kv_index)
+    vis = np.zeros((nq, nk), dtype=bool)
+    for i in range(nq):
+        b = i // q_block
+        n = int(kv_count[b]) if b < kv_count.shape[0] else 0
+        for t in range(max(0, min(n, kv_index.shape[1] if kv_index.ndim == 2 else 0))):
+            kb = int(kv_index[b, t])
+            if 0 <= kb and kb * k_block < nk:
+                vis[i, kb * k_block:min(nk, (kb + 1) * k_block)] = True
+    return vis
 
 
 def _row_blocks(nq: int, row_block):
@@ -69,7 +94,7 @@ def _row_blocks(nq: int, row_block):
         yield np.arange(r0, min(nq, r0 + rb))
 
 
-def attention_fwd(q, k, v, softmax_scale: float, causal: bool = False, row_block=None):
+def attention_fwd(q, k, v, softmax_scale: float, causal: bool = False, row_block=None, visible=None):
     """Dense definition of one head's forward pass.
 
     O_i = sum_j softmax_j(a_i) v_j with a_ij = scale * q_i . k_j (masked → -inf),
@@ -77,6 +102,8 @@ def attention_fwd(q, k, v, softmax_scale: float, causal: bool = False, row_block
     l_i = sum_j exp(a_ij - m_i), O_i = (sum_j exp(a_ij - m_i) v_j) / l_i,
     LSE_i = m_i + log l_i.  ``row_block`` only bounds memory: rows are
     independent, each row is still computed over all of its keys at once.
+    ``visible`` (bool [Nq, Nk], optional) masks further keys, e.g. a block-
+    sparse mask from :func:`block_sparse_visible`.
 
     Returns (O [Nq, d_v], LSE [Nq]) in fp64.
     """
@@ -87,7 +114,7 @@ def attention_fwd(q, k, v, softmax_scale: float, causal: bool = False, row_block
     if nq == 0 or nk == 0:
         return o, lse
     for rows in _row_blocks(nq, row_block):
-        a = _logits(q, k, softmax_scale, rows, nq, nk, causal)
+        a = _logits(q, k, softmax_scale, rows, nq, nk, causal, visible)
         m = a.max(axis=1)
         live = np.isfinite(m)
         if not live.any():
