@@ -24,7 +24,7 @@ _lib = _abi.load()
 SUPPORTED_HEAD_DIMS = ((64, 64), (128, 128), (192, 128))
 
 __all__ = [
-    "attn_fwd", "attn_fwd_varlen", "attn_bwd", "attn_bwd_varlen", "attn_exp2_eval",
+    "attn_fwd", "attn_fwd_block_sparse", "attn_fwd_varlen", "attn_bwd", "attn_bwd_varlen", "attn_exp2_eval",
     "attn_get_device_status", "attention", "AttnError", "SUPPORTED_HEAD_DIMS", "library_path",
 ]
 
@@ -112,6 +112,42 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool 
     p.exp2_emu_period = int(exp2_emu_period)
     ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_fwd(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_block_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_count: torch.Tensor,
+                          kv_index: torch.Tensor, *, causal: bool = False, softmax_scale: Optional[float] = None,
+                          out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                          stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Block-sparse dense forward. q/k/v as in :func:`attn_fwd`; kv_count int32 [ceil(Nq/256)] and
+    kv_index int32 [ceil(Nq/256), max_kv] (CUDA, contiguous): query block b (rows 256b..256b+255)
+    attends to key blocks (of 128 keys) kv_index[b, :kv_count[b]], each listed at most once.
+    Returns (O [B, Nq, H, d_v] bf16, LSE [B, H, Nq] fp32)."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_bf16(n, t, 4)
+    B, Nq, H, dqk = q.shape
+    Nk, dv = k.shape[1], v.shape[-1]
+    if k.shape != (B, Nk, H, dqk) or v.shape[:3] != (B, Nk, H):
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    nqb = (Nq + 255) // 256
+    for n, t in (("kv_count", kv_count), ("kv_index", kv_index)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    if kv_count.shape != (nqb,) or kv_index.dim() != 2 or kv_index.shape[0] != nqb:
+        raise ValueError(f"kv_count must be [{nqb}] and kv_index [{nqb}, max_kv]")
+    scale = float(softmax_scale) if softmax_scale is not None else 1.0 / math.sqrt(dqk)
+    if out is None:
+        out = torch.empty((B, Nq, H, dv), dtype=torch.bfloat16, device=q.device)
+    _check_bf16("out", out, 4)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if lse.shape != (B, H, Nq) or not lse.is_contiguous() or lse.dtype != torch.float32:
+        raise ValueError("lse must be a contiguous float32 [B, H, Nq] tensor")
+    p = AttnFwdParams()
+    _fill_fwd(p, q, k, v, out, lse, _strides4, scale, causal)
+    p.batch, p.seqlen_q, p.seqlen_k = B, Nq, Nk
+    _abi.check(_lib.attn_fwd_block_sparse(ctypes.byref(p), _ptr(kv_count), _ptr(kv_index), int(kv_index.shape[1]),
+                                          _stream(stream)), "attn_fwd_block_sparse")
     return out, lse
 
 

@@ -159,7 +159,14 @@ attn_status_t check_fwd(const attn_fwd_params* p, bool varlen) {
   return ATTN_OK;
 }
 
-attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream) {
+// Block-sparse key lists (nullptr kv_count: dense or varlen attention).
+struct SparseSpec {
+  const int32_t* kv_count = nullptr;
+  const int32_t* kv_index = nullptr;
+  int32_t max_kv = 0;
+};
+
+attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream, const SparseSpec& sp = {}) {
   ATTN_TRY(check_fwd(p, varlen));
   if (p->exp2_emu_period != 0 && p->exp2_emu_period != 4 && p->exp2_emu_period != 8) return ATTN_ERR_INVALID_ARG;
   const int nq_rows = varlen ? p->total_q : p->seqlen_q;
@@ -192,6 +199,9 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
   a.causal = p->causal ? 1 : 0;
   a.stats = p->rescale_stats;
   a.emu_period = p->exp2_emu_period;
+  a.kv_count = sp.kv_count;
+  a.kv_index = sp.kv_index;
+  a.max_kv = sp.max_kv;
   cudaError_t e = status_ptr(&a.status);
   if (e != cudaSuccess) return cuda_fail(e, "status word");
 
@@ -215,7 +225,8 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
                     p->k_head_stride, 128));
   ATTN_TRY(make_map(&tv, p->v, p->d_v, p->heads, nk_rows, nb, p->v_batch_stride, p->v_row_stride,
                     p->v_head_stride, 128));
-  e = launch_fwd(p->d_qk, p->d_v, tq, tk, tv, a, stream);
+  e = sp.kv_count ? launch_fwd_sparse(p->d_qk, p->d_v, tq, tk, tv, a, stream)
+                  : launch_fwd(p->d_qk, p->d_v, tq, tk, tv, a, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "fwd launch");
 }
 
@@ -338,6 +349,23 @@ attn_status_t attn_fwd_varlen(const attn_fwd_params* p, void* workspace, size_t 
   (void)workspace;
   (void)workspace_bytes;
   return run_fwd(p, true, static_cast<cudaStream_t>(stream));
+}
+
+attn_status_t attn_fwd_block_sparse(const attn_fwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
+                                    int32_t max_kv, attn_stream_t stream) {
+  ATTN_TRY(check_fwd(p, false));
+  if (p->exp2_emu_period != 0) return ATTN_ERR_INVALID_ARG;
+  const int64_t n_qblk = (static_cast<int64_t>(p->seqlen_q) + 255) / 256;
+  if (max_kv < 0 || n_qblk * max_kv > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
+  if (n_qblk > 0) {
+    if (!kv_count || (reinterpret_cast<uintptr_t>(kv_count) & 3u)) return ATTN_ERR_INVALID_ARG;
+    if (max_kv > 0 && (!kv_index || (reinterpret_cast<uintptr_t>(kv_index) & 3u))) return ATTN_ERR_INVALID_ARG;
+  }
+  SparseSpec sp;
+  sp.kv_count = kv_count;
+  sp.kv_index = kv_index;
+  sp.max_kv = max_kv;
+  return run_fwd(p, false, static_cast<cudaStream_t>(stream), sp);
 }
 
 size_t attn_bwd_workspace_size(const attn_bwd_params* p) {

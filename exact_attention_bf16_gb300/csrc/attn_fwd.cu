@@ -81,7 +81,11 @@ __device__ __forceinline__ int key_limit(int row, int nq, int nk, int causal) {
   return lim < 0 ? 0 : (lim > nk ? nk : lim);
 }
 
-template <int DQK, int DV, int EMU_PERIOD>
+// SPARSE: the CTA's key blocks are the list a.kv_index[mblk * a.max_kv + j],
+// j < a.kv_count[mblk], instead of 0 .. nkv-1 (block-sparse masks, the
+// FlexAttention / block-sparse variants of wittx "FlashAttention-4", section
+// Python写GPU内核); the causal mask still applies inside the listed blocks.
+template <int DQK, int DV, int EMU_PERIOD, bool SPARSE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const FwdArgs a) {
@@ -112,16 +116,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (row0 >= nq) return;  // block-uniform: this unit is shorter than the grid's longest
 
   int nkv[QT];
+  if constexpr (SPARSE) {
+    int n = a.kv_count[mblk];
+    n = n < 0 ? 0 : (n > a.max_kv ? a.max_kv : n);
 #pragma unroll
-  for (int i = 0; i < QT; ++i) {
-    const int r = row0 + i * BM;
-    if (r >= nq) {
-      nkv[i] = 0;
-    } else {
-      const int last = min(r + BM - 1, nq - 1);
-      nkv[i] = ceil_div(key_limit(last, nq, nk, a.causal), BN);
+    for (int i = 0; i < QT; ++i) nkv[i] = row0 + i * BM < nq ? n : 0;
+  } else {
+#pragma unroll
+    for (int i = 0; i < QT; ++i) {
+      const int r = row0 + i * BM;
+      if (r >= nq) {
+        nkv[i] = 0;
+      } else {
+        const int last = min(r + BM - 1, nq - 1);
+        nkv[i] = ceil_div(key_limit(last, nq, nk, a.causal), BN);
+      }
     }
   }
+  // Key block of step j: j itself, or the j-th listed block. A listed index
+  // outside [0, ceil(nk / BN)) becomes ceil(nk / BN), a block past the last
+  // key: its loads read zeros and every key in it is masked. (Addresses and
+  // bounds are rebuilt from the kernel arguments to keep registers free.)
+  auto key_block = [&](int j) -> int {
+    if constexpr (SPARSE) {
+      const int n_kblk = ceil_div(a.seqlen_k, BN);
+      const int kb = __ldg(a.kv_index + (mblk * a.max_kv + j));  // the host keeps the product below 2^31
+      return (kb < 0 || kb >= n_kblk) ? n_kblk : kb;
+    } else {
+      return j;
+    }
+  };
   const int nkv_max = max(nkv[0], nkv[1]);
 
   const uint32_t warp = warp_id(), lane = lane_id();
@@ -164,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       bool ok = true;
       for (int j = 0; j < nkv_max && ok; ++j) {
+        const int kb = key_block(j);
         for (int which = 0; which < 2 && ok; ++which) {
           const int u = 2 * j + which;
           const int slot = u % C::NSLOT;
@@ -174,11 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (which == 0) {
             mbar_arrive_expect_tx(&bar->kv_full[slot], C::K_BYTES);
             for (int c = 0; c < C::QCH; ++c)
-              tma_load_4d(dst + c * kChunk, &tmk, &bar->kv_full[slot], c * 64, h, k_start + j * BN, b);
+              tma_load_4d(dst + c * kChunk, &tmk, &bar->kv_full[slot], c * 64, h, k_start + kb * BN, b);
           } else {
             mbar_arrive_expect_tx(&bar->kv_full[slot], C::V_BYTES);
             for (int c = 0; c < C::VCH; ++c)
-              tma_load_4d(dst + c * kChunk, &tmv, &bar->kv_full[slot], c * 64, h, k_start + j * BN, b);
+              tma_load_4d(dst + c * kChunk, &tmv, &bar->kv_full[slot], c * 64, h, k_start + kb * BN, b);
           }
           ++issued;
         }
@@ -259,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n_rescale = 0, n_opp = 0;
     bool ok = true;
     for (int j = 0; j < nkv[i]; ++j) {
+      const int kb = key_block(j);  // read before the wait, off the critical path
       ok = mbar_wait_warp(&bar->s_full[i], static_cast<uint32_t>(j) & 1u, a.status, 0x300 + i);
       if (!ok) break;
       tc_fence_after();
@@ -268,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(lane_base + tS(i) + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
       tmem_ld32(lane_base + tS(i) + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
       tmem_wait_ld();
-      const int cnt = lim - j * BN;  // visible keys of this row inside tile j
+      const int cnt = lim - kb * BN;  // visible keys of this row inside the tile
       if (cnt < BN) {
 #pragma unroll
         for (int c = 0; c < BN; ++c)
@@ -408,11 +434,11 @@ __global__ void exp2_eval_kernel(const float* x, float* yp, float* yh, int64_t n
   }
 }
 
-template <int DQK, int DV, int EMU>
+template <int DQK, int DV, int EMU, bool SPARSE = false>
 cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
                      cudaStream_t stream) {
   using C = Cfg<DQK, DV>;
-  auto kern = attn_fwd_kernel<DQK, DV, EMU>;
+  auto kern = attn_fwd_kernel<DQK, DV, EMU, SPARSE>;
   static PerDeviceOnce once;
   cudaError_t e = once.run([&]() -> cudaError_t {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -451,6 +477,16 @@ cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorM
   if (d_qk == 64 && d_v == 64) return fwd::launch_t<64, 64>(tq, tk, tv, a, stream);
   if (d_qk == 128 && d_v == 128) return fwd::launch_t<128, 128>(tq, tk, tv, a, stream);
   if (d_qk == 192 && d_v == 128) return fwd::launch_t<192, 128>(tq, tk, tv, a, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_sparse(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const FwdArgs& a, cudaStream_t stream) {
+  if (a.cu_q != nullptr || a.emu_period != 0 || a.kv_count == nullptr || a.max_kv < 0) return cudaErrorInvalidValue;
+  if (a.max_kv > 0 && a.kv_index == nullptr) return cudaErrorInvalidValue;
+  if (d_qk == 64 && d_v == 64) return fwd::launch_e<64, 64, 0, true>(tq, tk, tv, a, stream);
+  if (d_qk == 128 && d_v == 128) return fwd::launch_e<128, 128, 0, true>(tq, tk, tv, a, stream);
+  if (d_qk == 192 && d_v == 128) return fwd::launch_e<192, 128, 0, true>(tq, tk, tv, a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -45,10 +45,20 @@ struct FwdArgs {
   uint32_t* status;          // device status word
   unsigned long long* stats; // optional rescale counters
   int emu_period;            // exp2: every emu_period-th column on the FMA pipe (0 = none)
+  // Block-sparse forward only (nullptr otherwise): for 256-row query block b,
+  // kv_count[b] key blocks of 128 keys, listed at kv_index[b * max_kv + j].
+  const int* kv_count;
+  const int* kv_index;
+  int max_kv;
 };
 
 cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& a, cudaStream_t stream);
+
+// Block-sparse forward (dense layout, cu_q == nullptr, emu_period == 0): the
+// same kernel walking a.kv_index's key blocks instead of 0 .. nkv-1.
+cudaError_t launch_fwd_sparse(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const FwdArgs& a, cudaStream_t stream);
 
 // Fills O = 0 and LSE = -inf for rows that see no key at all (Nk == 0).
 cudaError_t launch_fwd_empty(const FwdArgs& a, int d_v, cudaStream_t stream);

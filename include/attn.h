@@ -149,6 +149,23 @@ size_t attn_bwd_workspace_size(const attn_bwd_params* p);
 
 /* Dense forward: O, LSE from Q, K, V. */
 attn_status_t attn_fwd(const attn_fwd_params* p, void* workspace, size_t workspace_bytes, attn_stream_t stream);
+/* Block-sparse forward (the FlexAttention / block-sparse variants named in
+ * wittx "FlashAttention-4", section Python写GPU内核): the dense forward
+ * restricted to listed key blocks. Dense layout only (cu_seqlens NULL),
+ * exp2_emu_period must be 0. Query rows form blocks of 256 (block b = rows
+ * 256b .. 256b+255), keys blocks of 128. Query block b attends to the key
+ * blocks kv_index[b * max_kv + j] for j < kv_count[b]; every other key is
+ * masked, and `causal` still applies inside the listed blocks. kv_count
+ * (int32[ceil(seqlen_q / 256)]) and kv_index (int32[ceil(seqlen_q / 256) *
+ * max_kv]) are device arrays owned by the caller, shared by every (batch,
+ * head), 4-byte aligned; ceil(seqlen_q / 256) * max_kv < 2^31. Counts are
+ * clamped to [0, max_kv]; indices outside [0, ceil(seqlen_k / 128)) list
+ * nothing; a block listed twice for one query block is counted twice (the
+ * caller lists each at most once). Rows that see no key get O = 0,
+ * LSE = -inf. Bad arguments give ATTN_ERR_INVALID_ARG before any launch.
+ * There is no block-sparse backward. */
+attn_status_t attn_fwd_block_sparse(const attn_fwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
+                                    int32_t max_kv, attn_stream_t stream);
 /* Variable-length forward (cu_seqlens_q / cu_seqlens_k required). */
 attn_status_t attn_fwd_varlen(const attn_fwd_params* p, void* workspace, size_t workspace_bytes,
                               attn_stream_t stream);

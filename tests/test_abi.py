@@ -120,3 +120,25 @@ def test_product_path_does_not_import_the_oracle(_abi):
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(root, f), encoding="utf-8").read()
                 assert "oracle" not in src.replace("CPU oracle", ""), f
+
+
+def _valid_sparse_args():
+    return 0x20000, 0x30000, 3  # kv_count, kv_index (dummy aligned device addresses), max_kv
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda p, a: (p, (a[0], a[1], -1)), INVALID),                   # negative max_kv
+    (lambda p, a: (p, (None, a[1], a[2])), INVALID),                 # no counts
+    (lambda p, a: (p, (a[0], None, a[2])), INVALID),                 # no index array with max_kv > 0
+    (lambda p, a: (p, (a[0] + 2, a[1], a[2])), INVALID),             # misaligned counts
+    (lambda p, a: (p, (a[0], a[1] + 1, a[2])), INVALID),             # misaligned indices
+    (lambda p, a: (p, (a[0], a[1], 0x7fffffff)), INVALID),           # n_qblk * max_kv overflows int32
+    (lambda p, a: (setattr(p, "exp2_emu_period", 4) or p, a), INVALID),  # exp2 emulation not built here
+    (lambda p, a: (setattr(p, "cu_seqlens_q", 0x10000) or p, a), INVALID),  # dense layout only
+    (lambda p, a: (setattr(p, "d_qk", 96) or p, a), UNSUPPORTED),
+])
+def test_block_sparse_rejects_bad_arguments_without_a_gpu(lib, _abi, mutate, expect):
+    p = _valid_fwd(_abi)
+    p.seqlen_q = 600  # three query blocks of 256 rows
+    p, (cnt, idx, max_kv) = mutate(p, _valid_sparse_args())
+    assert lib.attn_fwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, None) == expect
