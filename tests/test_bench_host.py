@@ -95,3 +95,11 @@ def test_multi_rank_timing_reduction_gloo():
 def test_bench_rejects_short_warmup():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "1"])
+
+
+def test_causal_pair_count_matches_brute_force():
+    import workloads
+    for nq, nk in [(2048, 8192), (8192, 2048), (5, 3), (3, 5), (1, 1000), (1000, 1), (513, 700)]:
+        brute = sum(min(max(i + nk - nq + 1, 0), nk) for i in range(nq))
+        assert workloads.causal_pairs(nq, nk) == brute
+    assert workloads.causal_pairs(8192, 8192) == 8192 * 8192 / 2  # the half-square convention

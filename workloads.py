@@ -171,9 +171,20 @@ def sample_pairs(batch: int, heads: int, n: int, seed: int = 1234):
 # Work counting (a measurement convention, not part of the computation)
 # ---------------------------------------------------------------------------
 def causal_pairs(nq: int, nk: int) -> float:
-    """Visible (query, key) pairs under the bottom-right causal mask, counted
-    by the usual half-square convention when nq == nk."""
-    return nq * nk / 2.0
+    """Visible (query, key) pairs under the bottom-right causal mask: row i sees
+    clip(i + nk - nq + 1, 0, nk) keys. When nq == nk the usual half-square
+    convention nq * nk / 2 is used instead of the exact nq (nq + 1) / 2."""
+    if nq == nk:
+        return nq * nk / 2.0
+    lo, hi = nk - nq + 1, nk  # the first and last row's unclipped counts
+
+    def tri(x):  # 1 + 2 + ... + x
+        return x * (x + 1) // 2 if x > 0 else 0
+
+    a, b = max(lo, 1), min(hi, nk)
+    ramp = tri(b) - tri(a - 1) if a <= b else 0  # rows with 1 .. nk visible keys
+    full = max(0, hi - max(lo, nk + 1) + 1) * nk  # rows past the last key see all nk
+    return float(ramp + full)
 
 
 def attn_flops(nq: int, nk: int, d_qk: int, d_v: int, causal: bool, direction: str = "fwd") -> float:
