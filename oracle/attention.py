@@ -126,12 +126,13 @@ def attention_fwd(q, k, v, softmax_scale: float, causal: bool = False, row_block
     return o, lse
 
 
-def attention_bwd(q, k, v, do, softmax_scale: float, causal: bool = False, row_block=None):
+def attention_bwd(q, k, v, do, softmax_scale: float, causal: bool = False, row_block=None, visible=None):
     """Dense definition of one head's backward pass for the loss <O, dO>.
 
     P_ij = exp(a_ij - LSE_i); dV_j = sum_i P_ij dO_i; dP_ij = dO_i . v_j;
     D_i = sum_j P_ij dP_ij; dS_ij = P_ij (dP_ij - D_i);
     dQ_i = scale * sum_j dS_ij k_j; dK_j = scale * sum_i dS_ij q_i.
+    ``visible`` masks further keys as in :func:`attention_fwd` (P_ij = 0 there).
 
     Returns dict with dq, dk, dv (fp64) and D (the row term, computed as
     sum_j P_ij dP_ij so that tests can check it against dO_i . O_i).
@@ -145,7 +146,7 @@ def attention_bwd(q, k, v, do, softmax_scale: float, causal: bool = False, row_b
     if nq == 0 or nk == 0:
         return {"dq": dq, "dk": dk, "dv": dv, "D": D}
     for rows in _row_blocks(nq, row_block):
-        a = _logits(q, k, softmax_scale, rows, nq, nk, causal)
+        a = _logits(q, k, softmax_scale, rows, nq, nk, causal, visible)
         m = a.max(axis=1)
         live = np.isfinite(m)
         if not live.any():

@@ -81,3 +81,35 @@ def test_causal_and_block_mask_combine_brute_force():
         ref = [sum(w[t] * v[js[t], c] for t in range(len(js))) / s for c in range(2)]
         assert abs(lse[i] - (m + math.log(s))) < 1e-12
         np.testing.assert_allclose(o[i], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_backward_all_blocks_listed_is_the_dense_result():
+    from oracle import attention_bwd
+    nq, nk = 300, 260
+    q, k, v, do = rand(nq, 5), rand(nk, 5, seed=11), rand(nk, 3, seed=12), rand(nq, 3, seed=13)
+    nkb = math.ceil(nk / 128)
+    cnt = np.full(math.ceil(nq / 256), nkb)
+    vis = block_sparse_visible(nq, nk, cnt, np.tile(np.arange(nkb), (cnt.shape[0], 1)))
+    for causal in (False, True):
+        g1 = attention_bwd(q, k, v, do, 0.6, causal, visible=vis)
+        g0 = attention_bwd(q, k, v, do, 0.6, causal)
+        for n in ("dq", "dk", "dv"):
+            assert np.array_equal(g1[n], g0[n])
+
+
+@pytest.mark.parametrize("blocks", [[1], [0, 2], [2, 0]])
+def test_backward_equals_gradients_over_the_sliced_keys(blocks):
+    # one query block listing some key blocks: dQ, and dK/dV on the listed keys, are the
+    # gradients of attention over those keys alone; every other key gets zero gradient
+    from oracle import attention_bwd
+    nq, nk = 180, 300
+    q, k, v, do = rand(nq, 4), rand(nk, 4, seed=14), rand(nk, 3, seed=15), rand(nq, 3, seed=16)
+    vis = block_sparse_visible(nq, nk, [len(blocks)], [blocks])
+    keys = np.concatenate([np.arange(b * 128, min(nk, (b + 1) * 128)) for b in sorted(blocks)])
+    g = attention_bwd(q, k, v, do, 0.8, False, visible=vis)
+    r = attention_bwd(q, k[keys], v[keys], do, 0.8, False)
+    np.testing.assert_allclose(g["dq"], r["dq"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(g["dk"][keys], r["dk"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(g["dv"][keys], r["dv"], rtol=1e-11, atol=1e-12)
+    rest = np.setdiff1d(np.arange(nk), keys)
+    assert np.all(g["dk"][rest] == 0) and np.all(g["dv"][rest] == 0)
