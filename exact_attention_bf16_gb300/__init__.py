@@ -24,7 +24,7 @@ _lib = _abi.load()
 SUPPORTED_HEAD_DIMS = ((64, 64), (128, 128), (192, 128))
 
 __all__ = [
-    "attn_fwd", "attn_fwd_block_sparse", "attn_fwd_varlen", "attn_bwd", "attn_bwd_varlen", "attn_exp2_eval",
+    "attn_fwd", "attn_fwd_block_sparse", "attn_fwd_varlen", "attn_bwd", "attn_bwd_block_sparse", "attn_bwd_varlen", "attn_exp2_eval",
     "attn_get_device_status", "attention", "AttnError", "SUPPORTED_HEAD_DIMS", "library_path",
 ]
 
@@ -229,6 +229,35 @@ def attn_bwd(q, k, v, out, lse, dout, *, causal: bool = False, softmax_scale: Op
             p.phase_events[i] = h
     ws, nbytes = _workspace(_lib.attn_bwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_bwd(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_block_sparse(q, k, v, out, lse, dout, kv_count, kv_index, *, causal: bool = False,
+                          softmax_scale: Optional[float] = None, deterministic: bool = False, dq=None, dk=None,
+                          dv=None, stream=None):
+    """Block-sparse backward for :func:`attn_fwd_block_sparse` with the same kv_count / kv_index:
+    returns (dQ, dK, dV) bf16 for the loss <O, dO>."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _check_bf16(n, t, 4)
+    B, Nq, H, dqk = q.shape
+    Nk = k.shape[1]
+    nqb = (Nq + 255) // 256
+    for n, t in (("kv_count", kv_count), ("kv_index", kv_index)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    if kv_count.shape != (nqb,) or kv_index.dim() != 2 or kv_index.shape[0] != nqb:
+        raise ValueError(f"kv_count must be [{nqb}] and kv_index [{nqb}, max_kv]")
+    scale = float(softmax_scale) if softmax_scale is not None else 1.0 / math.sqrt(dqk)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    p = AttnBwdParams()
+    _fill_fwd(p.fwd, q, k, v, out, lse, _strides4, scale, causal)
+    p.fwd.batch, p.fwd.seqlen_q, p.fwd.seqlen_k = B, Nq, Nk
+    _fill_bwd(p, dout, dq, dk, dv, _strides4, deterministic)
+    ws, nbytes = _workspace(_lib.attn_bwd_block_sparse_workspace_size(ctypes.byref(p)), q.device)
+    _abi.check(_lib.attn_bwd_block_sparse(ctypes.byref(p), _ptr(kv_count), _ptr(kv_index), int(kv_index.shape[1]),
+                                          _ptr(ws), nbytes, _stream(stream)), "attn_bwd_block_sparse")
     return dq, dk, dv
 
 

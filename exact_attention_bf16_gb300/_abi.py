@@ -76,6 +76,9 @@ def load(path: str = LIB_PATH):
         "attn_fwd": (ctypes.c_int, [P(AttnFwdParams), c_vp, ctypes.c_size_t, c_vp]),
         "attn_fwd_varlen": (ctypes.c_int, [P(AttnFwdParams), c_vp, ctypes.c_size_t, c_vp]),
         "attn_fwd_block_sparse": (ctypes.c_int, [P(AttnFwdParams), c_vp, c_vp, ctypes.c_int32, c_vp]),
+        "attn_bwd_block_sparse_workspace_size": (ctypes.c_size_t, [P(AttnBwdParams)]),
+        "attn_bwd_block_sparse": (ctypes.c_int, [P(AttnBwdParams), c_vp, c_vp, ctypes.c_int32, c_vp,
+                                                 ctypes.c_size_t, c_vp]),
         "attn_bwd": (ctypes.c_int, [P(AttnBwdParams), c_vp, ctypes.c_size_t, c_vp]),
         "attn_bwd_varlen": (ctypes.c_int, [P(AttnBwdParams), c_vp, ctypes.c_size_t, c_vp]),
         "attn_bwd_noalloc": (ctypes.c_int, [P(AttnBwdParams), c_vp]),

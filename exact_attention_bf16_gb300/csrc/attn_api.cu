@@ -240,7 +240,16 @@ size_t bwd_workspace_bytes(const attn_bwd_params* p, bool varlen) {
   return static_cast<size_t>((rows * 4 + 255) / 256 * 256);
 }
 
-attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool varlen, cudaStream_t stream) {
+// Extra workspace of the block-sparse backward: the transposed lists
+// (int32 q_count[n_kb], then q_index[n_kb][n_qb256]) after the D vector.
+size_t bwd_sparse_extra_bytes(const attn_fwd_params& f) {
+  const int64_t n_kb = (static_cast<int64_t>(f.seqlen_k) + 127) / 128;
+  const int64_t n_qb = (static_cast<int64_t>(f.seqlen_q) + 255) / 256;
+  return static_cast<size_t>((n_kb * 4 + 255) / 256 * 256 + (n_kb * n_qb * 4 + 255) / 256 * 256);
+}
+
+attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool varlen, cudaStream_t stream,
+                      const SparseSpec& sp = {}) {
   if (!p) return ATTN_ERR_INVALID_ARG;
   const attn_fwd_params& f = p->fwd;
   ATTN_TRY(check_fwd(&f, varlen));
@@ -256,7 +265,8 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
     cudaError_t be = bind_device_of(nq_rows ? f.q : f.k);
     if (be != cudaSuccess) return be == cudaErrorInvalidDevicePointer ? ATTN_ERR_INVALID_ARG : cuda_fail(be, "device");
   }
-  const size_t need = bwd_workspace_bytes(p, varlen);
+  const size_t need_d = bwd_workspace_bytes(p, varlen);
+  const size_t need = need_d + (sp.kv_count ? bwd_sparse_extra_bytes(f) : 0);
   if (nq_rows > 0 && nk_rows > 0 && (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u)))
     return ATTN_ERR_WORKSPACE;
 
@@ -290,6 +300,16 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
   a.scale = f.softmax_scale;
   a.scale_log2 = f.softmax_scale * 1.4426950408889634f;
   a.causal = f.causal ? 1 : 0;
+  const int n_kb_sparse = (f.seqlen_k + 127) / 128;
+  if (sp.kv_count) {
+    a.kv_count = sp.kv_count;
+    a.kv_index = sp.kv_index;
+    a.max_kv = sp.max_kv;
+    a.n_qb256 = (f.seqlen_q + 255) / 256;
+    uint8_t* extra = static_cast<uint8_t*>(ws) + need_d;
+    a.q_count = reinterpret_cast<int*>(extra);
+    a.q_index = reinterpret_cast<int*>(extra + (static_cast<size_t>(n_kb_sparse) * 4 + 255) / 256 * 256);
+  }
   cudaError_t e = status_ptr(&a.status);
   if (e != cudaSuccess) return cuda_fail(e, "status word");
 
@@ -315,6 +335,7 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
     return p->phase_events[i] ? cudaEventRecord(static_cast<cudaEvent_t>(p->phase_events[i]), stream) : cudaSuccess;
   };
   e = launch_bwd_preprocess(f.d_v, a, stream);
+  if (e == cudaSuccess && sp.kv_count) e = launch_bwd_transpose_lists(a, n_kb_sparse, stream);
   if (e == cudaSuccess) e = mark(0);
   if (e != cudaSuccess) return cuda_fail(e, "bwd preprocess launch");
   e = launch_bwd_dkdv(f.d_qk, f.d_v, tq2, tk, tv, tdo2, a, stream);
@@ -366,6 +387,29 @@ attn_status_t attn_fwd_block_sparse(const attn_fwd_params* p, const int32_t* kv_
   sp.kv_index = kv_index;
   sp.max_kv = max_kv;
   return run_fwd(p, false, static_cast<cudaStream_t>(stream), sp);
+}
+
+size_t attn_bwd_block_sparse_workspace_size(const attn_bwd_params* p) {
+  if (!p || p->fwd.cu_seqlens_q != nullptr) return 0;
+  return bwd_workspace_bytes(p, false) + bwd_sparse_extra_bytes(p->fwd);
+}
+
+attn_status_t attn_bwd_block_sparse(const attn_bwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
+                                    int32_t max_kv, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  if (!p) return ATTN_ERR_INVALID_ARG;
+  ATTN_TRY(check_fwd(&p->fwd, false));
+  const int64_t n_qblk = (static_cast<int64_t>(p->fwd.seqlen_q) + 255) / 256;
+  const int64_t n_kblk = (static_cast<int64_t>(p->fwd.seqlen_k) + 127) / 128;
+  if (max_kv < 0 || n_qblk * max_kv > 0x7fffffff || n_qblk * n_kblk > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
+  if (n_qblk > 0) {
+    if (!kv_count || (reinterpret_cast<uintptr_t>(kv_count) & 3u)) return ATTN_ERR_INVALID_ARG;
+    if (max_kv > 0 && (!kv_index || (reinterpret_cast<uintptr_t>(kv_index) & 3u))) return ATTN_ERR_INVALID_ARG;
+  }
+  SparseSpec sp;
+  sp.kv_count = kv_count;
+  sp.kv_index = kv_index;
+  sp.max_kv = max_kv;
+  return run_bwd(p, workspace, workspace_bytes, false, static_cast<cudaStream_t>(stream), sp);
 }
 
 size_t attn_bwd_workspace_size(const attn_bwd_params* p) {

@@ -179,7 +179,9 @@ struct DkdvBars {
   uint32_t tmem_base;
 };
 
-template <int DQK, int DV>
+// SPARSE: the key block's query tiles are those of the query blocks in its
+// transposed block-sparse list (a.q_index), not m_begin .. m_end - 1.
+template <int DQK, int DV, bool SPARSE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo, const BwdArgs a) {
@@ -208,7 +210,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     m_begin = i_min > 0 ? i_min / QB : 0;
   }
   const int m_end = ceil_div(U.nq, QB);
-  const int T = m_end > m_begin ? m_end - m_begin : 0;
+  int T = m_end > m_begin ? m_end - m_begin : 0;
+  if constexpr (SPARSE) T = __ldg(a.q_count + n) * (256 / QB);
+  // first query row of step t
+  auto q_row = [&](int t) -> int {
+    if constexpr (SPARSE) {
+      constexpr int R = 256 / QB;  // query tiles per 256-row block
+      return __ldg(a.q_index + (n * a.n_qb256 + t / R)) * 256 + (t % R) * QB;
+    } else {
+      return (m_begin + t) * QB;
+    }
+  };
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -252,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < T && ok; ++t) {
       const int st = t % C::NST;
       const uint32_t use = static_cast<uint32_t>(t / C::NST);
-      const int tile = (m_begin + t) * QB;
+      const int tile = q_row(t);
       // fetch the vectors first, so their latency overlaps the wait for the slot
       float nl[QB / 32], nd[QB / 32];
 #pragma unroll
@@ -404,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(&bar->kv_tmem);
     const float2 sl2v = make_float2(sl2, sl2);
     for (int t = 0; t < T && ok; ++t) {
-      const int q0 = (m_begin + t) * QB;
+      const int q0 = q_row(t);
       ok = mbar_wait_warp(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1300);
       // this tile's (-LSE*log2e, -D) vectors, written by the loader lanes
       if (ok) ok = mbar_wait_warp(&bar->st_full[t % C::NST], static_cast<uint32_t>(t / C::NST) & 1u, a.status, 0x1302);
@@ -546,6 +558,7 @@ struct DkdvWBars {
 };
 static_assert(sizeof(DkdvWBars) <= 256, "dK/dV barriers must fit their reserved bytes");
 
+template <bool SPARSE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_wide_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo, const BwdArgs a) {
@@ -576,7 +589,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     m_begin = i_min > 0 ? i_min / QB : 0;
   }
   const int m_end = ceil_div(U.nq, QB);
-  const int T = m_end > m_begin ? m_end - m_begin : 0;
+  int T = m_end > m_begin ? m_end - m_begin : 0;
+  if constexpr (SPARSE) T = __ldg(a.q_count + n) * (256 / QB);
+  // first query row of step t
+  auto q_row = [&](int t) -> int {
+    if constexpr (SPARSE) {
+      constexpr int R = 256 / QB;  // query tiles per 256-row block
+      return __ldg(a.q_index + (n * a.n_qb256 + t / R)) * 256 + (t % R) * QB;
+    } else {
+      return (m_begin + t) * QB;
+    }
+  };
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -623,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nq_issued = 0, ng_issued = 0;
     bool ok = true;
     for (int t = 0; t < T && ok; ++t) {
-      const int tile = (m_begin + t) * QB;
+      const int tile = q_row(t);
       const int row = U.q_start + tile;
       float nl[QB / 32], nd[QB / 32];  // fetched first, so their latency overlaps the waits below
 #pragma unroll
@@ -782,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto lanes = [&](int lg) { return tbase + ((quarter * 32u + 16u * static_cast<uint32_t>(lg)) << 16); };
     bool ok = true;
     for (int t = 0; t < T && ok; ++t) {
-      const int q0 = (m_begin + t) * QB + 64 * wg;  // this warpgroup's first query
+      const int q0 = q_row(t) + 64 * wg;  // this warpgroup's first query
       const uint32_t col = region(t) + 64 * wg;
       // ---- phase A: P from S^T(t), written over S^T(t) as bf16 P^T
       ok = mbar_wait_warp(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1430) &&
@@ -951,7 +974,10 @@ __device__ __forceinline__ int key_limit(int row, int nq, int nk, int causal) {
   return lim < 0 ? 0 : (lim > nk ? nk : lim);
 }
 
-template <int DQK, int DV>
+// SPARSE: the query tile's key blocks are its 256-row query block's list
+// (a.kv_index), not 0 .. T - 1; an index outside [0, ceil(nk / KB)) becomes a
+// block past the last key (zero loads, every key masked).
+template <int DQK, int DV, bool SPARSE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
               const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo, const BwdArgs a) {
@@ -972,7 +998,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = m * MB;
   if (q0 >= U.nq) return;
   const int last = min(q0 + MB - 1, U.nq - 1);
-  const int T = ceil_div(key_limit(last, U.nq, U.nk, a.causal), KB);
+  int T = ceil_div(key_limit(last, U.nq, U.nk, a.causal), KB);
+  if constexpr (SPARSE) {
+    const int c = __ldg(a.kv_count + (q0 >> 8));
+    T = c < 0 ? 0 : (c > a.max_kv ? a.max_kv : c);
+  }
+  // key block of step t
+  auto key_block = [&](int t) -> int {
+    if constexpr (SPARSE) {
+      const int n_kb = ceil_div(U.nk, KB);
+      const int kb = __ldg(a.kv_index + ((q0 >> 8) * a.max_kv + t));
+      return (kb < 0 || kb >= n_kb) ? n_kb : kb;
+    } else {
+      return t;
+    }
+  };
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -1013,7 +1053,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nk_issued = 0, nv_issued = 0;
       bool ok = true;
       for (int t = 0; t < T && ok; ++t) {
-        const int row = U.k_start + t * KB;
+        const int row = U.k_start + key_block(t) * KB;
         const int ks = t % C::KST, vs = t % C::VST;
         ok = mbar_wait(&bar->k_empty[ks], (static_cast<uint32_t>(t / C::KST) & 1u) ^ 1u, a.status, 0x2100 + ks);
         if (!ok) break;
@@ -1141,7 +1181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait_warp(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2300);
       if (!ok) break;
       tc_fence_after();
-      const int cnt = lim - t * KB;  // visible keys of this row in tile t
+      const int cnt = lim - key_block(t) * KB;  // visible keys of this row in tile t
       // copy this warpgroup's 64 columns of S and dP out of TMEM, then release dP
       uint32_t s[64], dp[64];
       tmem_ld32(lane_base + C::tS + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
@@ -1222,16 +1262,39 @@ __global__ void zero_kernel(void* base, int64_t sb, int64_t sn, int64_t sh, int 
   }
 }
 
+// Transposed block lists: one warp per key block n scans the query blocks in
+// 32-wide groups, ascending, and appends those whose list holds n (a block
+// listed twice counts once). Deterministic: no atomics, fixed order.
+__global__ void transpose_lists_kernel(BwdArgs a, int n_kb) {
+  const int n = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = static_cast<int>(threadIdx.x & 31u);
+  if (n >= n_kb) return;  // whole warps
+  int count = 0;
+  for (int b0 = 0; b0 < a.n_qb256; b0 += 32) {
+    const int b = b0 + lane;
+    bool hit = false;
+    if (b < a.n_qb256) {
+      int c = a.kv_count[b];
+      c = c < 0 ? 0 : (c > a.max_kv ? a.max_kv : c);
+      for (int j = 0; j < c && !hit; ++j) hit = a.kv_index[b * a.max_kv + j] == n;
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, hit);
+    if (hit) const_cast<int*>(a.q_index)[n * a.n_qb256 + count + __popc(m & ((1u << lane) - 1u))] = b;
+    count += __popc(m);
+  }
+  if (lane == 0) const_cast<int*>(a.q_count)[n] = count;
+}
+
 template <typename K>
 cudaError_t set_smem(K kern, int bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int DQK, int DV>
+template <int DQK, int DV, bool SPARSE>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                           const BwdArgs& a, cudaStream_t stream) {
   using C = DkdvCfg<DQK, DV>;
-  auto kern = dkdv_kernel<DQK, DV>;
+  auto kern = dkdv_kernel<DQK, DV, SPARSE>;
   static PerDeviceOnce once;
   cudaError_t e = once.run([&] { return set_smem(kern, C::SMEM); });
   if (e != cudaSuccess) return e;
@@ -1242,23 +1305,24 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   return cudaGetLastError();
 }
 
+template <bool SPARSE>
 cudaError_t launch_dkdv_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
   static PerDeviceOnce once;
-  cudaError_t e = once.run([] { return set_smem(dkdv_wide_kernel, DkdvWCfg::SMEM); });
+  cudaError_t e = once.run([] { return set_smem(dkdv_wide_kernel<SPARSE>, DkdvWCfg::SMEM); });
   if (e != cudaSuccess) return e;
   const int64_t grid = static_cast<int64_t>(a.n_kblk) * a.num_units * a.heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  dkdv_wide_kernel<<<static_cast<unsigned>(grid), kThreads, DkdvWCfg::SMEM, stream>>>(tq, tk, tv, tdo, a);
+  dkdv_wide_kernel<SPARSE><<<static_cast<unsigned>(grid), kThreads, DkdvWCfg::SMEM, stream>>>(tq, tk, tv, tdo, a);
   return cudaGetLastError();
 }
 
-template <int DQK, int DV>
+template <int DQK, int DV, bool SPARSE>
 cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                         const BwdArgs& a, cudaStream_t stream) {
   using C = DqCfg<DQK, DV>;
-  auto kern = dq_kernel<DQK, DV>;
+  auto kern = dq_kernel<DQK, DV, SPARSE>;
   static PerDeviceOnce once;
   cudaError_t e = once.run([&] { return set_smem(kern, C::SMEM); });
   if (e != cudaSuccess) return e;
@@ -1285,17 +1349,39 @@ cudaError_t launch_bwd_preprocess(int d_v, const BwdArgs& a, cudaStream_t stream
 
 cudaError_t launch_bwd_dkdv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
-  if (d_qk == 64 && d_v == 64) return bwd::launch_dkdv_t<64, 64>(tq, tk, tv, tdo, a, stream);
-  if (d_qk == 128 && d_v == 128) return bwd::launch_dkdv_wide(tq, tk, tv, tdo, a, stream);
-  if (d_qk == 192 && d_v == 128) return bwd::launch_dkdv_t<192, 128>(tq, tk, tv, tdo, a, stream);
+  if (a.kv_count != nullptr) {
+    if (a.cu_q != nullptr || a.q_count == nullptr || a.q_index == nullptr) return cudaErrorInvalidValue;
+    if (d_qk == 64 && d_v == 64) return bwd::launch_dkdv_t<64, 64, true>(tq, tk, tv, tdo, a, stream);
+    if (d_qk == 128 && d_v == 128) return bwd::launch_dkdv_wide<true>(tq, tk, tv, tdo, a, stream);
+    if (d_qk == 192 && d_v == 128) return bwd::launch_dkdv_t<192, 128, true>(tq, tk, tv, tdo, a, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (d_qk == 64 && d_v == 64) return bwd::launch_dkdv_t<64, 64, false>(tq, tk, tv, tdo, a, stream);
+  if (d_qk == 128 && d_v == 128) return bwd::launch_dkdv_wide<false>(tq, tk, tv, tdo, a, stream);
+  if (d_qk == 192 && d_v == 128) return bwd::launch_dkdv_t<192, 128, false>(tq, tk, tv, tdo, a, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_transpose_lists(const BwdArgs& a, int n_kb, cudaStream_t stream) {
+  if (n_kb <= 0) return cudaSuccess;
+  const int64_t threads = static_cast<int64_t>(n_kb) * 32;
+  const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+  bwd::transpose_lists_kernel<<<blocks, 256, 0, stream>>>(a, n_kb);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
-  if (d_qk == 64 && d_v == 64) return bwd::launch_dq_t<64, 64>(tq, tk, tv, tdo, a, stream);
-  if (d_qk == 128 && d_v == 128) return bwd::launch_dq_t<128, 128>(tq, tk, tv, tdo, a, stream);
-  if (d_qk == 192 && d_v == 128) return bwd::launch_dq_t<192, 128>(tq, tk, tv, tdo, a, stream);
+  if (a.kv_count != nullptr) {
+    if (a.cu_q != nullptr) return cudaErrorInvalidValue;
+    if (d_qk == 64 && d_v == 64) return bwd::launch_dq_t<64, 64, true>(tq, tk, tv, tdo, a, stream);
+    if (d_qk == 128 && d_v == 128) return bwd::launch_dq_t<128, 128, true>(tq, tk, tv, tdo, a, stream);
+    if (d_qk == 192 && d_v == 128) return bwd::launch_dq_t<192, 128, true>(tq, tk, tv, tdo, a, stream);
+    return cudaErrorInvalidValue;
+  }
+  if (d_qk == 64 && d_v == 64) return bwd::launch_dq_t<64, 64, false>(tq, tk, tv, tdo, a, stream);
+  if (d_qk == 128 && d_v == 128) return bwd::launch_dq_t<128, 128, false>(tq, tk, tv, tdo, a, stream);
+  if (d_qk == 192 && d_v == 128) return bwd::launch_dq_t<192, 128, false>(tq, tk, tv, tdo, a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -89,13 +89,27 @@ struct BwdArgs {
   float scale_log2;  // softmax_scale * log2(e)
   int causal;
   uint32_t* status;
+  // Block-sparse backward only (nullptr otherwise). Forward lists, for the dQ
+  // kernel: 256-row query block b sees key blocks kv_index[b * max_kv + j],
+  // j < kv_count[b]. Transposed lists, for the dK/dV kernel: key block n is
+  // seen by query blocks q_index[n * n_qb256 + j], j < q_count[n], ascending.
+  const int* kv_count;
+  const int* kv_index;
+  int max_kv;
+  const int* q_count;
+  const int* q_index;
+  int n_qb256;
 };
 
 // D = rowsum(dO * O) into args.dsum.
 cudaError_t launch_bwd_preprocess(int d_v, const BwdArgs& a, cudaStream_t stream);
-// dK, dV (KV-stationary) and dQ (Q-stationary). Maps: q, k, v, dO.
+// dK, dV (KV-stationary) and dQ (Q-stationary). Maps: q, k, v, dO. With
+// a.kv_count set they walk the block-sparse lists (dense layout only).
 cudaError_t launch_bwd_dkdv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+// Builds a.q_count / a.q_index (transposed block lists) from a.kv_count / a.kv_index
+// for n_kb key blocks, deterministically (ascending query blocks).
+cudaError_t launch_bwd_transpose_lists(const BwdArgs& a, int n_kb, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
 // Zero-fills dQ, dK, dV rows of a problem with no keys or no queries.

@@ -163,7 +163,7 @@ attn_status_t attn_fwd(const attn_fwd_params* p, void* workspace, size_t workspa
  * nothing; a block listed twice for one query block is counted twice (the
  * caller lists each at most once). Rows that see no key get O = 0,
  * LSE = -inf. Bad arguments give ATTN_ERR_INVALID_ARG before any launch.
- * There is no block-sparse backward. */
+ * The gradients come from attn_bwd_block_sparse. */
 attn_status_t attn_fwd_block_sparse(const attn_fwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
                                     int32_t max_kv, attn_stream_t stream);
 /* Variable-length forward (cu_seqlens_q / cu_seqlens_k required). */
@@ -174,6 +174,15 @@ attn_status_t attn_bwd(const attn_bwd_params* p, void* workspace, size_t workspa
 /* Variable-length backward. */
 attn_status_t attn_bwd_varlen(const attn_bwd_params* p, void* workspace, size_t workspace_bytes,
                               attn_stream_t stream);
+
+/* Block-sparse backward: the gradients of attn_fwd_block_sparse for the same
+ * kv_count / kv_index / max_kv (same rules; dense layout only). The key
+ * blocks' transposed lists are built on the stream into the workspace, whose
+ * size is attn_bwd_block_sparse_workspace_size(p) (16-byte aligned). Both
+ * modes are bitwise reproducible, as for attn_bwd. */
+size_t attn_bwd_block_sparse_workspace_size(const attn_bwd_params* p);
+attn_status_t attn_bwd_block_sparse(const attn_bwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
+                                    int32_t max_kv, void* workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /* Backward for callers that cannot allocate device memory (an engine that
  * plans all memory up front and forbids later cudaMalloc, a plugin that is

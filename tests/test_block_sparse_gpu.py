@@ -107,3 +107,56 @@ def test_sliding_window_sampled(ea):
     for b, r in enumerate(rows):
         idx[b, :len(r)] = r
     run_sparse(ea, w, cnt, idx, pairs=[(0, 0), (1, 5)])
+
+
+def run_sparse_bwd(ea, w, cnt, idx, pairs=None):
+    from oracle import attention_bwd
+    from parity import check_grads
+    t = workloads.make_dense(w, device="cuda", with_do=True)
+    kc = torch.from_numpy(cnt).cuda()
+    ki = torch.from_numpy(idx).cuda()
+    o, lse = ea.attn_fwd_block_sparse(t["q"], t["k"], t["v"], kc, ki, causal=w.causal, softmax_scale=w.scale)
+    dq, dk, dv = ea.attn_bwd_block_sparse(t["q"], t["k"], t["v"], o, lse, t["do"], kc, ki, causal=w.causal,
+                                          softmax_scale=w.scale)
+    dq2, dk2, dv2 = ea.attn_bwd_block_sparse(t["q"], t["k"], t["v"], o, lse, t["do"], kc, ki, causal=w.causal,
+                                             softmax_scale=w.scale, deterministic=True)
+    torch.cuda.synchronize()
+    assert ea.attn_get_device_status() == 0
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)  # reproducible
+    vis = block_sparse_visible(w.seqlen_q, w.seqlen_k, cnt, idx)
+    q, k, v, do = (t[n].cpu() for n in ("q", "k", "v", "do"))
+    pairs = pairs or [(b, h) for b in range(w.batch) for h in range(w.heads)]
+    for b, h in pairs:
+        ref = attention_bwd(q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h], w.scale, w.causal, row_block=1024,
+                            visible=vis)
+        check_grads({"dq": dq[b, :, h], "dk": dk[b, :, h], "dv": dv[b, :, h]}, ref, f"{w.name} b{b} h{h}")
+    return t, o, lse, (dq, dk, dv)
+
+
+@pytest.mark.parametrize("dims", DIMS)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("nq,nk,density", [(300, 700, 0.5), (1000, 260, 0.6), (513, 1100, 0.3)])
+def test_backward_random_block_lists(ea, dims, causal, nq, nk, density):
+    dqk, dv = dims
+    w = workloads.Workload("bsb", 2, 2, nq, nk, dqk, dv, causal, seed=nq + 3 * nk + dqk)
+    cnt, idx = random_lists(nq, nk, density, seed=nq * 5 + nk, extra={0: []})
+    run_sparse_bwd(ea, w, cnt, idx)
+
+
+@pytest.mark.parametrize("dims", DIMS)
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_every_block_listed_matches_the_dense_backward_bitwise(ea, dims, causal):
+    # extra listed blocks the dense walk skips are fully masked and add exact zeros
+    dqk, dv = dims
+    nq = nk = 1000
+    w = workloads.Workload("ball", 2, 2, nq, nk, dqk, dv, causal, seed=4)
+    nqb, nkb = math.ceil(nq / 256), math.ceil(nk / 128)
+    cnt = np.full(nqb, nkb, dtype=np.int32)
+    if causal:
+        cnt = np.array([math.ceil(min(nk, 256 * (b + 1)) / 128) for b in range(nqb)], dtype=np.int32)
+    idx = np.tile(np.arange(nkb, dtype=np.int32), (nqb, 1))
+    t, o, lse, (dq, dk, dv_) = run_sparse_bwd(ea, w, cnt, idx, pairs=[(1, 1)])
+    o_d, l_d = ea.attn_fwd(t["q"], t["k"], t["v"], causal=causal, softmax_scale=w.scale)
+    g = ea.attn_bwd(t["q"], t["k"], t["v"], o_d, l_d, t["do"], causal=causal, softmax_scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(dq, g[0]) and torch.equal(dk, g[1]) and torch.equal(dv_, g[2])
