@@ -40,8 +40,8 @@ WORKLOAD = dict(batch=4, heads=16, seqlen=8192, d_qk=128, d_v=128)
 # Measured on the non-causal B=2, H=16, N=8192 case (profiles/*_B2H16N8192.md) and
 # scaled x2 to the benchmark's B=4 launch (traffic grows with the (batch, head) units).
 KERNEL_TRAFFIC_NCU = {
-    "dkdv_wide_kernel": {"source_sha": "c84cb542be2f329c", "bytes_per_launch": 2 * (270.917376e6 + 104.7552e6)},
-    "dq_kernel": {"source_sha": "c84cb542be2f329c", "bytes_per_launch": 2 * (270.679808e6 + 52.036608e6)},
+    "dkdv_wide_kernel": {"source_sha": "e77285092c7bbf99", "bytes_per_launch": 2 * (270.671104e6 + 104.739584e6)},
+    "dq_kernel": {"source_sha": "e77285092c7bbf99", "bytes_per_launch": 2 * (270.743296e6 + 49.364736e6)},
     "attn_fwd_kernel": {"source_sha": "7b89da9206a28ab1", "bytes_per_launch": 2 * (201.413632e6 + 45.540608e6)},
 }
 
