@@ -305,20 +305,32 @@ def attn_get_device_status(stream=None) -> int:
 
 class _Attention(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, causal, softmax_scale, deterministic):
-        o, lse = attn_fwd(q, k, v, causal=causal, softmax_scale=softmax_scale)
+    def forward(ctx, q, k, v, causal, softmax_scale, deterministic, kv_count, kv_index):
+        if kv_count is None:
+            o, lse = attn_fwd(q, k, v, causal=causal, softmax_scale=softmax_scale)
+        else:
+            o, lse = attn_fwd_block_sparse(q, k, v, kv_count, kv_index, causal=causal, softmax_scale=softmax_scale)
         ctx.save_for_backward(q, k, v, o, lse)
         ctx.causal, ctx.scale, ctx.det = causal, softmax_scale, deterministic
+        ctx.lists = (kv_count, kv_index)
         return o
 
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, lse = ctx.saved_tensors
-        dq, dk, dv = attn_bwd(q, k, v, o, lse, do.contiguous(), causal=ctx.causal, softmax_scale=ctx.scale,
-                              deterministic=ctx.det)
-        return dq, dk, dv, None, None, None
+        kv_count, kv_index = ctx.lists
+        if kv_count is None:
+            dq, dk, dv = attn_bwd(q, k, v, o, lse, do.contiguous(), causal=ctx.causal, softmax_scale=ctx.scale,
+                                  deterministic=ctx.det)
+        else:
+            dq, dk, dv = attn_bwd_block_sparse(q, k, v, o, lse, do.contiguous(), kv_count, kv_index,
+                                               causal=ctx.causal, softmax_scale=ctx.scale, deterministic=ctx.det)
+        return dq, dk, dv, None, None, None, None, None
 
 
-def attention(q, k, v, causal: bool = False, softmax_scale: Optional[float] = None, deterministic: bool = False):
-    """Autograd wrapper over attn_fwd / attn_bwd for [B, N, H, d] bf16 tensors."""
-    return _Attention.apply(q, k, v, causal, softmax_scale, deterministic)
+def attention(q, k, v, causal: bool = False, softmax_scale: Optional[float] = None, deterministic: bool = False,
+              block_mask: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+    """Autograd wrapper over attn_fwd / attn_bwd for [B, N, H, d] bf16 tensors. ``block_mask``
+    = (kv_count, kv_index) selects the block-sparse pair attn_fwd_block_sparse / attn_bwd_block_sparse."""
+    kv_count, kv_index = block_mask if block_mask is not None else (None, None)
+    return _Attention.apply(q, k, v, causal, softmax_scale, deterministic, kv_count, kv_index)

@@ -160,3 +160,20 @@ def test_backward_every_block_listed_matches_the_dense_backward_bitwise(ea, dims
     g = ea.attn_bwd(t["q"], t["k"], t["v"], o_d, l_d, t["do"], causal=causal, softmax_scale=w.scale)
     torch.cuda.synchronize()
     assert torch.equal(dq, g[0]) and torch.equal(dk, g[1]) and torch.equal(dv_, g[2])
+
+
+def test_autograd_block_mask(ea):
+    # the autograd wrapper routes a block mask to the block-sparse forward and backward
+    nq = nk = 600
+    w = workloads.Workload("ag", 1, 2, nq, nk, 128, 128, True, seed=8)
+    cnt, idx = random_lists(nq, nk, 0.5, seed=77)
+    t = workloads.make_dense(w, device="cuda", with_do=True)
+    q, k, v = (t[n].clone().requires_grad_(True) for n in ("q", "k", "v"))
+    kc, ki = torch.from_numpy(cnt).cuda(), torch.from_numpy(idx).cuda()
+    o = ea.attention(q, k, v, causal=True, block_mask=(kc, ki))
+    o.backward(t["do"])
+    o2, l2 = ea.attn_fwd_block_sparse(t["q"], t["k"], t["v"], kc, ki, causal=True)
+    g = ea.attn_bwd_block_sparse(t["q"], t["k"], t["v"], o2, l2, t["do"], kc, ki, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o.detach(), o2)
+    assert torch.equal(q.grad, g[0]) and torch.equal(k.grad, g[1]) and torch.equal(v.grad, g[2])
