@@ -24,7 +24,8 @@ _lib = _abi.load()
 SUPPORTED_HEAD_DIMS = ((64, 64), (128, 128), (192, 128))
 
 __all__ = [
-    "attn_fwd", "attn_fwd_block_sparse", "attn_fwd_varlen", "attn_bwd", "attn_bwd_block_sparse", "attn_bwd_varlen", "attn_exp2_eval",
+    "attn_fwd", "attn_fwd_block_sparse", "attn_fwd_varlen", "attn_bwd", "attn_bwd_block_sparse",
+    "block_lists_from_mask", "attn_bwd_varlen", "attn_exp2_eval",
     "attn_get_device_status", "attention", "AttnError", "SUPPORTED_HEAD_DIMS", "library_path",
 ]
 
@@ -113,6 +114,21 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool 
     ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_fwd(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_fwd")
     return out, lse
+
+
+def block_lists_from_mask(block_mask: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    """(kv_count, kv_index) for :func:`attn_fwd_block_sparse` from a boolean block mask
+    [ceil(Nq/256), ceil(Nk/128)] (True = the query block attends to the key block), key blocks in
+    ascending order; on the mask's device. Argument preparation only."""
+    if block_mask.dtype != torch.bool or block_mask.dim() != 2:
+        raise ValueError("block_mask must be a 2-D bool tensor [query blocks, key blocks]")
+    m = block_mask.to(torch.int32)
+    kv_count = m.sum(dim=1, dtype=torch.int32)
+    max_kv = max(int(kv_count.max().item()) if kv_count.numel() else 0, 1)
+    # stable sort puts listed blocks first, each group in ascending key-block order
+    order = torch.sort(1 - m, dim=1, stable=True).indices.to(torch.int32)
+    kv_index = order[:, :max_kv].contiguous()
+    return kv_count.contiguous(), kv_index
 
 
 def attn_fwd_block_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_count: torch.Tensor,
