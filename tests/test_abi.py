@@ -142,3 +142,30 @@ def test_block_sparse_rejects_bad_arguments_without_a_gpu(lib, _abi, mutate, exp
     p.seqlen_q = 600  # three query blocks of 256 rows
     p, (cnt, idx, max_kv) = mutate(p, _valid_sparse_args())
     assert lib.attn_fwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, None) == expect
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda p, a: (p, (a[0], a[1], -1)), INVALID),
+    (lambda p, a: (p, (None, a[1], a[2])), INVALID),
+    (lambda p, a: (p, (a[0], None, a[2])), INVALID),
+    (lambda p, a: (p, (a[0] + 2, a[1], a[2])), INVALID),
+    (lambda p, a: (setattr(p.fwd, "cu_seqlens_q", 0x10000) or p, a), INVALID),
+    (lambda p, a: (setattr(p.fwd, "d_qk", 96) or p, a), UNSUPPORTED),
+])
+def test_block_sparse_backward_rejects_bad_arguments_without_a_gpu(lib, _abi, mutate, expect):
+    p = _abi.AttnBwdParams()
+    p.fwd = _valid_fwd(_abi)
+    p.fwd.seqlen_q = 600
+    p, (cnt, idx, max_kv) = mutate(p, _valid_sparse_args())
+    assert lib.attn_bwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, None, 0, None) == expect
+
+
+def test_block_sparse_backward_workspace_size(lib, _abi):
+    p = _abi.AttnBwdParams()
+    p.fwd = _valid_fwd(_abi)
+    p.fwd.seqlen_q, p.fwd.seqlen_k = 600, 1000  # 3 query blocks of 256, 8 key blocks of 128
+    dense = lib.attn_bwd_workspace_size(ctypes.byref(p))
+    sparse = lib.attn_bwd_block_sparse_workspace_size(ctypes.byref(p))
+    assert sparse >= dense + 8 * 4 + 8 * 3 * 4  # q_count[8] and q_index[8][3] on top of the D vector
+    p.fwd.cu_seqlens_q = 0x10000
+    assert lib.attn_bwd_block_sparse_workspace_size(ctypes.byref(p)) == 0  # dense layout only
