@@ -169,3 +169,16 @@ def test_block_sparse_backward_workspace_size(lib, _abi):
     assert sparse >= dense + 8 * 4 + 8 * 3 * 4  # q_count[8] and q_index[8][3] on top of the D vector
     p.fwd.cu_seqlens_q = 0x10000
     assert lib.attn_bwd_block_sparse_workspace_size(ctypes.byref(p)) == 0  # dense layout only
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++17")])
+def test_header_compiles_as_c_and_cpp(lang, std):
+    import shutil
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    src = '#include "attn.h"\nint main(void) { return (int)sizeof(attn_fwd_params) == 0; }\n'
+    r = subprocess.run([cc, "-x", lang, std, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-I", inc, "-"],
+                       input=src, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
