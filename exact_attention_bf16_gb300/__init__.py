@@ -116,6 +116,14 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool 
     return out, lse
 
 
+def _check_lists(q: torch.Tensor, kv_count: torch.Tensor, kv_index: torch.Tensor):
+    for n, t in (("kv_count", kv_count), ("kv_index", kv_index)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+        if t.device != q.device:
+            raise ValueError(f"{n} is on {t.device} but q is on {q.device}: the block lists must be on q's GPU")
+
+
 def block_lists_from_mask(block_mask: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
     """(kv_count, kv_index) for :func:`attn_fwd_block_sparse` from a boolean block mask
     [ceil(Nq/256), ceil(Nk/128)] (True = the query block attends to the key block), key blocks in
@@ -146,9 +154,7 @@ def attn_fwd_block_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_
     if k.shape != (B, Nk, H, dqk) or v.shape[:3] != (B, Nk, H):
         raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
     nqb = (Nq + 255) // 256
-    for n, t in (("kv_count", kv_count), ("kv_index", kv_index)):
-        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    _check_lists(q, kv_count, kv_index)
     if kv_count.shape != (nqb,) or kv_index.dim() != 2 or kv_index.shape[0] != nqb:
         raise ValueError(f"kv_count must be [{nqb}] and kv_index [{nqb}, max_kv]")
     scale = float(softmax_scale) if softmax_scale is not None else 1.0 / math.sqrt(dqk)
@@ -258,9 +264,7 @@ def attn_bwd_block_sparse(q, k, v, out, lse, dout, kv_count, kv_index, *, causal
     B, Nq, H, dqk = q.shape
     Nk = k.shape[1]
     nqb = (Nq + 255) // 256
-    for n, t in (("kv_count", kv_count), ("kv_index", kv_index)):
-        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    _check_lists(q, kv_count, kv_index)
     if kv_count.shape != (nqb,) or kv_index.dim() != 2 or kv_index.shape[0] != nqb:
         raise ValueError(f"kv_count must be [{nqb}] and kv_index [{nqb}, max_kv]")
     scale = float(softmax_scale) if softmax_scale is not None else 1.0 / math.sqrt(dqk)

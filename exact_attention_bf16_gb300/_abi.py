@@ -83,6 +83,7 @@ def load(path: str = LIB_PATH):
         "attn_bwd_varlen": (ctypes.c_int, [P(AttnBwdParams), c_vp, ctypes.c_size_t, c_vp]),
         "attn_bwd_noalloc": (ctypes.c_int, [P(AttnBwdParams), c_vp]),
         "attn_exp2_eval": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i64, c_vp]),
+        "attn_diag_wait_timeout": (ctypes.c_int, [P(AttnFwdParams), ctypes.c_uint32, c_vp]),
         "attn_get_device_status": (ctypes.c_int, [c_vp, P(ctypes.c_uint32)]),
         "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "attn_last_cuda_error": (ctypes.c_char_p, []),

@@ -91,17 +91,57 @@ attn_status_t make_map(CUtensorMap* m, const void* base, int d, int n_heads, int
   return ATTN_OK;
 }
 
-// Makes the device that owns `ptr` current for this library's runtime on the
-// calling thread (entry points may be called from threads, such as an
-// autograd worker, on which this library has not yet touched the device).
-cudaError_t bind_device_of(const void* ptr) {
+}  // namespace
+
+// DeviceScope (kernels.h): makes the data's device current for the launches of
+// one entry point and restores the caller's current device afterwards.
+// Entry points may be called from threads, such as an autograd worker, on
+// which this library has not yet touched the device, and from multi-GPU
+// callers whose current device must survive the call.
+cudaError_t DeviceScope::bind(const void* ptr) {
   cudaPointerAttributes attr{};
   cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
   if (e != cudaSuccess) return e;
   if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return cudaErrorInvalidDevicePointer;
+  e = cudaGetDevice(&prev_);
+  if (e != cudaSuccess) return e;
+  device_ = attr.device;
+  if (prev_ == device_) return cudaSuccess;
   // cudaSetDevice also makes the device's primary context current on this thread.
-  return cudaSetDevice(attr.device);
+  e = cudaSetDevice(device_);
+  if (e == cudaSuccess) switched_ = true;
+  return e;
 }
+
+DeviceScope::~DeviceScope() {
+  if (!switched_) return;
+  // Put the caller's device back only if its primary context already exists:
+  // selecting a device whose context was never created would create one (and
+  // take its memory) on a GPU the caller never used.
+  using GetFn = CUresult (*)(CUdevice*, int);
+  using StateFn = CUresult (*)(CUdevice, unsigned int*, int*);
+  static GetFn get = nullptr;
+  static StateFn state = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuDeviceGet", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get = reinterpret_cast<GetFn>(f);
+    if (cudaGetDriverEntryPointByVersion("cuDevicePrimaryCtxGetState", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      state = reinterpret_cast<StateFn>(f);
+  });
+  CUdevice dev;
+  unsigned int flags = 0;
+  int active = 0;
+  if (get && state && get(&dev, prev_) == CUDA_SUCCESS && state(dev, &flags, &active) == CUDA_SUCCESS && active)
+    cudaSetDevice(prev_);
+}
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool stride_ok(int64_t s) { return s >= 0 && (s % 8) == 0 && s < (int64_t(1) << 38); }
@@ -159,6 +199,22 @@ attn_status_t check_fwd(const attn_fwd_params* p, bool varlen) {
   return ATTN_OK;
 }
 
+// The block lists must be device memory on the same GPU as the data: a list
+// on another GPU would be read across devices by the kernels.
+attn_status_t check_lists_device(const void* data, const int32_t* kv_count, const int32_t* kv_index) {
+  if (!data) return ATTN_OK;  // no rows: nothing is launched
+  cudaPointerAttributes ad{}, ac{}, ai{};
+  if (cudaPointerGetAttributes(&ad, data) != cudaSuccess) return ATTN_ERR_INVALID_ARG;
+  for (const int32_t* p : {kv_count, kv_index}) {
+    if (!p) continue;
+    cudaPointerAttributes& at = p == kv_count ? ac : ai;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) return ATTN_ERR_INVALID_ARG;
+    if ((at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) || at.device != ad.device)
+      return ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_OK;
+}
+
 // Block-sparse key lists (nullptr kv_count: dense or varlen attention).
 struct SparseSpec {
   const int32_t* kv_count = nullptr;
@@ -166,7 +222,9 @@ struct SparseSpec {
   int32_t max_kv = 0;
 };
 
-attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream, const SparseSpec& sp = {}) {
+// diag_limit != 0: the diagnostic launch of attn_diag_wait_timeout instead of the forward.
+attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream, const SparseSpec& sp = {},
+                      uint32_t diag_limit = 0) {
   ATTN_TRY(check_fwd(p, varlen));
   if (p->exp2_emu_period != 0 && p->exp2_emu_period != 4 && p->exp2_emu_period != 8) return ATTN_ERR_INVALID_ARG;
   const int nq_rows = varlen ? p->total_q : p->seqlen_q;
@@ -174,8 +232,9 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
   const int units = varlen ? p->num_seqs : p->batch;
   const int max_q = varlen ? p->max_seqlen_q : p->seqlen_q;
   if (nq_rows == 0 || max_q == 0) return ATTN_OK;
+  DeviceScope scope;
   {
-    cudaError_t be = bind_device_of(p->q ? p->q : p->k);
+    cudaError_t be = scope.bind(p->q ? p->q : p->k);
     if (be != cudaSuccess) return be == cudaErrorInvalidDevicePointer ? ATTN_ERR_INVALID_ARG : cuda_fail(be, "device");
   }
 
@@ -202,6 +261,7 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
   a.kv_count = sp.kv_count;
   a.kv_index = sp.kv_index;
   a.max_kv = sp.max_kv;
+  a.spin_limit = diag_limit;
   cudaError_t e = status_ptr(&a.status);
   if (e != cudaSuccess) return cuda_fail(e, "status word");
 
@@ -225,16 +285,19 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
                     p->k_head_stride, 128));
   ATTN_TRY(make_map(&tv, p->v, p->d_v, p->heads, nk_rows, nb, p->v_batch_stride, p->v_row_stride,
                     p->v_head_stride, 128));
-  e = sp.kv_count ? launch_fwd_sparse(p->d_qk, p->d_v, tq, tk, tv, a, stream)
-                  : launch_fwd(p->d_qk, p->d_v, tq, tk, tv, a, stream);
+  e = diag_limit ? launch_fwd_diag_timeout(tq, tk, tv, a, stream)
+      : sp.kv_count ? launch_fwd_sparse(p->d_qk, p->d_v, tq, tk, tv, a, stream)
+                    : launch_fwd(p->d_qk, p->d_v, tq, tk, tv, a, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "fwd launch");
 }
 
 
 int bwd_dkdv_rows(int d_qk) { return d_qk == 128 ? 128 : 64; }  // query rows per step of the dK/dV kernel
 
+// Invalid (negative) shapes need no workspace: the call itself reports them.
 size_t bwd_workspace_bytes(const attn_bwd_params* p, bool varlen) {
   const attn_fwd_params& f = p->fwd;
+  if (f.heads < 0 || (varlen ? f.total_q < 0 : (f.batch < 0 || f.seqlen_q < 0))) return 0;
   const int64_t rows = varlen ? static_cast<int64_t>(f.heads) * f.total_q
                               : static_cast<int64_t>(f.batch) * f.heads * f.seqlen_q;
   return static_cast<size_t>((rows * 4 + 255) / 256 * 256);
@@ -261,8 +324,9 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
   const int nq_rows = varlen ? f.total_q : f.seqlen_q;
   const int nk_rows = varlen ? f.total_k : f.seqlen_k;
   if (nq_rows == 0 && nk_rows == 0) return ATTN_OK;
+  DeviceScope scope;
   {
-    cudaError_t be = bind_device_of(nq_rows ? f.q : f.k);
+    cudaError_t be = scope.bind(nq_rows ? f.q : f.k);
     if (be != cudaSuccess) return be == cudaErrorInvalidDevicePointer ? ATTN_ERR_INVALID_ARG : cuda_fail(be, "device");
   }
   const size_t need_d = bwd_workspace_bytes(p, varlen);
@@ -382,6 +446,7 @@ attn_status_t attn_fwd_block_sparse(const attn_fwd_params* p, const int32_t* kv_
     if (!kv_count || (reinterpret_cast<uintptr_t>(kv_count) & 3u)) return ATTN_ERR_INVALID_ARG;
     if (max_kv > 0 && (!kv_index || (reinterpret_cast<uintptr_t>(kv_index) & 3u))) return ATTN_ERR_INVALID_ARG;
   }
+  if (n_qblk > 0) ATTN_TRY(check_lists_device(p->q, kv_count, max_kv > 0 ? kv_index : nullptr));
   SparseSpec sp;
   sp.kv_count = kv_count;
   sp.kv_index = kv_index;
@@ -405,6 +470,7 @@ attn_status_t attn_bwd_block_sparse(const attn_bwd_params* p, const int32_t* kv_
     if (!kv_count || (reinterpret_cast<uintptr_t>(kv_count) & 3u)) return ATTN_ERR_INVALID_ARG;
     if (max_kv > 0 && (!kv_index || (reinterpret_cast<uintptr_t>(kv_index) & 3u))) return ATTN_ERR_INVALID_ARG;
   }
+  if (n_qblk > 0) ATTN_TRY(check_lists_device(p->fwd.q, kv_count, max_kv > 0 ? kv_index : nullptr));
   SparseSpec sp;
   sp.kv_count = kv_count;
   sp.kv_index = kv_index;
@@ -429,12 +495,21 @@ attn_status_t attn_bwd_varlen(const attn_bwd_params* p, void* workspace, size_t 
 attn_status_t attn_exp2_eval(const float* x, float* y_poly, float* y_hw, int64_t n, attn_stream_t stream) {
   if (n < 0 || (n > 0 && !x) || (!y_poly && !y_hw)) return ATTN_ERR_INVALID_ARG;
   if (n == 0) return ATTN_OK;
+  DeviceScope scope;
   {
-    cudaError_t be = bind_device_of(x);
+    cudaError_t be = scope.bind(x);
     if (be != cudaSuccess) return be == cudaErrorInvalidDevicePointer ? ATTN_ERR_INVALID_ARG : cuda_fail(be, "device");
   }
   cudaError_t e = launch_exp2_eval(x, y_poly, y_hw, n, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "exp2 eval launch");
+}
+
+attn_status_t attn_diag_wait_timeout(const attn_fwd_params* p, uint32_t spin_limit, attn_stream_t stream) {
+  ATTN_TRY(check_fwd(p, false));
+  if (p->d_qk != 64 || p->d_v != 64 || p->exp2_emu_period != 0) return ATTN_ERR_INVALID_ARG;
+  if (spin_limit < 1 || spin_limit > (1u << 20)) return ATTN_ERR_INVALID_ARG;
+  if (p->seqlen_q == 0 || p->seqlen_k == 0) return ATTN_ERR_INVALID_ARG;  // the kernel must launch
+  return run_fwd(p, false, static_cast<cudaStream_t>(stream), SparseSpec{}, spin_limit);
 }
 
 attn_status_t attn_get_device_status(attn_stream_t stream, uint32_t* detail) {

@@ -85,7 +85,12 @@ __device__ __forceinline__ int key_limit(int row, int nq, int nk, int causal) {
 // j < a.kv_count[mblk], instead of 0 .. nkv-1 (block-sparse masks, the
 // FlexAttention / block-sparse variants of wittx "FlashAttention-4", section
 // Python写GPU内核); the causal mask still applies inside the listed blocks.
-template <int DQK, int DV, int EMU_PERIOD, bool SPARSE = false>
+//
+// DIAG (diagnostic only, attn_diag_wait_timeout): the loader issues no copies
+// and every wait gives up after a.spin_limit polls, so the MMA and softmax
+// waits run out, record DEV_TIMEOUT_MBAR and the kernel returns with nothing
+// in flight (no copy or MMA was ever issued).
+template <int DQK, int DV, int EMU_PERIOD, bool SPARSE = false, bool DIAG = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const FwdArgs a) {
@@ -147,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   const int nkv_max = max(nkv[0], nkv[1]);
+  const uint32_t lim = DIAG ? a.spin_limit : kSpinLimit;  // poll limit of the waits below
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -176,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   regs_dec<C::REG_LO>();
   if (warp == 0) {
     // ======================= TMA producer ===================================
-    if (lane == 0) {
+    if (lane == 0 && !DIAG) {
       tma_prefetch_desc(&tmq);
       tma_prefetch_desc(&tmk);
       tma_prefetch_desc(&tmv);
@@ -221,14 +227,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(BM, DV, false, true);
-      bool ok = mbar_wait(&bar->q_full[0], 0, a.status, 0x200) && mbar_wait(&bar->q_full[1], 0, a.status, 0x201);
+      bool ok = mbar_wait(&bar->q_full[0], 0, a.status, 0x200, lim) &&
+                mbar_wait(&bar->q_full[1], 0, a.status, 0x201, lim);
       for (int j = 0; j <= nkv_max && ok; ++j) {
         const bool haveK = j < nkv_max;
         const bool haveV = j > 0;
         const int uK = 2 * j, uV = 2 * (j - 1) + 1;
         const int sK = uK % C::NSLOT, sV = (uV + C::NSLOT) % C::NSLOT;
-        if (haveK) ok = mbar_wait(&bar->kv_full[sK], static_cast<uint32_t>(uK / C::NSLOT) & 1u, a.status, 0x210);
-        if (ok && haveV) ok = mbar_wait(&bar->kv_full[sV], static_cast<uint32_t>(uV / C::NSLOT) & 1u, a.status, 0x211);
+        if (haveK) ok = mbar_wait(&bar->kv_full[sK], static_cast<uint32_t>(uK / C::NSLOT) & 1u, a.status, 0x210, lim);
+        if (ok && haveV)
+          ok = mbar_wait(&bar->kv_full[sV], static_cast<uint32_t>(uV / C::NSLOT) & 1u, a.status, 0x211, lim);
         if (!ok) break;
         tc_fence_after();
         // descriptors built once per tile, advanced per k-step with one add
@@ -238,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < QT; ++i) {
           if (haveV && j - 1 < nkv[i]) {
             // O_i (+)= P_i(j-1) V_{j-1}: P from TMEM (aliasing S_i), V MN-major in shared memory
-            ok = mbar_wait(&bar->p_full[i], static_cast<uint32_t>(j - 1) & 1u, a.status, 0x220 + i);
+            ok = mbar_wait(&bar->p_full[i], static_cast<uint32_t>(j - 1) & 1u, a.status, 0x220 + i, lim);
             if (!ok) break;
             tc_fence_after();
             const uint32_t acc0 = j - 1 > 0 ? 1u : 0u;
@@ -285,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < nkv[i]; ++j) {
       const int kb = key_block(j);  // read before the wait, off the critical path
-      ok = mbar_wait_warp(&bar->s_full[i], static_cast<uint32_t>(j) & 1u, a.status, 0x300 + i);
+      ok = mbar_wait_warp(&bar->s_full[i], static_cast<uint32_t>(j) & 1u, a.status, 0x300 + i, lim);
       if (!ok) break;
       tc_fence_after();
       uint32_t s[BN];
@@ -371,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue: O = acc / l (exact normalisation), LSE = ln2 * (m + log2 l)
     if (ok && nkv[i] > 0) {
-      ok = mbar_wait_warp(&bar->o_full[i], 0, a.status, 0x310 + i);
+      ok = mbar_wait_warp(&bar->o_full[i], 0, a.status, 0x310 + i, lim);
       tc_fence_after();
     }
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
@@ -434,11 +442,11 @@ __global__ void exp2_eval_kernel(const float* x, float* yp, float* yh, int64_t n
   }
 }
 
-template <int DQK, int DV, int EMU, bool SPARSE = false>
+template <int DQK, int DV, int EMU, bool SPARSE = false, bool DIAG = false>
 cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
                      cudaStream_t stream) {
   using C = Cfg<DQK, DV>;
-  auto kern = attn_fwd_kernel<DQK, DV, EMU, SPARSE>;
+  auto kern = attn_fwd_kernel<DQK, DV, EMU, SPARSE, DIAG>;
   static PerDeviceOnce once;
   cudaError_t e = once.run([&]() -> cudaError_t {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -488,6 +496,12 @@ cudaError_t launch_fwd_sparse(int d_qk, int d_v, const CUtensorMap& tq, const CU
   if (d_qk == 128 && d_v == 128) return fwd::launch_e<128, 128, 0, true>(tq, tk, tv, a, stream);
   if (d_qk == 192 && d_v == 128) return fwd::launch_e<192, 128, 0, true>(tq, tk, tv, a, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_diag_timeout(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                    const FwdArgs& a, cudaStream_t stream) {
+  if (a.cu_q != nullptr || a.kv_count != nullptr || a.spin_limit == 0) return cudaErrorInvalidValue;
+  return fwd::launch_e<64, 64, 0, false, true>(tq, tk, tv, a, stream);
 }
 
 cudaError_t launch_fwd_empty(const FwdArgs& a, int d_v, cudaStream_t stream) {

@@ -27,6 +27,7 @@
 #include <mutex>
 
 #include "../../include/attn.h"
+#include "kernels.h"
 
 namespace {
 
@@ -54,20 +55,26 @@ cudaError_t scratch_address(int dev, void** out) {
 
 extern "C" attn_status_t attn_bwd_noalloc(const attn_bwd_params* p, attn_stream_t stream) {
   if (!p) return ATTN_ERR_INVALID_ARG;
-  const bool varlen = p->fwd.cu_seqlens_q != nullptr;
+  const attn_fwd_params& f = p->fwd;
+  const bool varlen = f.cu_seqlens_q != nullptr;
+  // Shapes first: a negative size is a bad argument, not a problem too large
+  // for the scratch (attn_bwd_workspace_size reports 0 for it).
+  if (f.heads < 1 || (varlen ? (f.total_q < 0 || f.total_k < 0) : (f.batch < 1 || f.seqlen_q < 0 || f.seqlen_k < 0)))
+    return ATTN_ERR_INVALID_ARG;
   const size_t need = attn_bwd_workspace_size(p);
   if (need > ATTN_BWD_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;  // problem too large for the fixed scratch
-  const int nq = varlen ? p->fwd.total_q : p->fwd.seqlen_q;
-  const int nk = varlen ? p->fwd.total_k : p->fwd.seqlen_k;
+  const int nq = varlen ? f.total_q : f.seqlen_q;
+  const int nk = varlen ? f.total_k : f.seqlen_k;
   void* ws = nullptr;
   if (nq > 0 && nk > 0) {
-    // Set-up: make the data's device current, then resolve the array's address on it.
-    cudaPointerAttributes attr{};
-    if (!p->fwd.q || cudaPointerGetAttributes(&attr, p->fwd.q) != cudaSuccess ||
-        (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged))
-      return ATTN_ERR_INVALID_ARG;
-    if (cudaSetDevice(attr.device) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (scratch_address(attr.device, &ws) != cudaSuccess) return ATTN_ERR_CUDA;
+    // Set-up: with the data's device current, resolve the array's address on
+    // it; the caller's current device is restored when `scope` ends.
+    if (!f.q) return ATTN_ERR_INVALID_ARG;
+    gb300::DeviceScope scope;
+    const cudaError_t e = scope.bind(f.q);
+    if (e == cudaErrorInvalidDevicePointer) return ATTN_ERR_INVALID_ARG;
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    if (scratch_address(scope.device(), &ws) != cudaSuccess) return ATTN_ERR_CUDA;
   }
   return varlen ? attn_bwd_varlen(p, ws, ATTN_BWD_NOALLOC_SCRATCH_BYTES, stream)
                 : attn_bwd(p, ws, ATTN_BWD_NOALLOC_SCRATCH_BYTES, stream);

@@ -28,6 +28,26 @@ struct PerDeviceOnce {
   }
 };
 
+// Makes the device that owns a pointer current for the rest of a scope and
+// restores the calling thread's previous device when the scope ends (when
+// that device's context exists already, so no context is created on a GPU
+// the caller never used). Defined in attn_api.cu.
+class DeviceScope {
+ public:
+  DeviceScope() = default;
+  DeviceScope(const DeviceScope&) = delete;
+  DeviceScope& operator=(const DeviceScope&) = delete;
+  ~DeviceScope();
+  // cudaErrorInvalidDevicePointer if ptr is not device (or managed) memory.
+  cudaError_t bind(const void* ptr);
+  int device() const { return device_; }
+
+ private:
+  int prev_ = -1;
+  int device_ = -1;
+  bool switched_ = false;
+};
+
 // Forward kernel arguments (passed by value; tensor maps go separately as
 // __grid_constant__ parameters).
 struct FwdArgs {
@@ -50,6 +70,7 @@ struct FwdArgs {
   const int* kv_count;
   const int* kv_index;
   int max_kv;
+  uint32_t spin_limit;       // diagnostic launches only: poll limit of every wait
 };
 
 cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -59,6 +80,11 @@ cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorM
 // same kernel walking a.kv_index's key blocks instead of 0 .. nkv-1.
 cudaError_t launch_fwd_sparse(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const FwdArgs& a, cudaStream_t stream);
+
+// Diagnostic: the d = 64 dense forward with no copies issued and every wait
+// limited to a.spin_limit polls (attn_diag_wait_timeout).
+cudaError_t launch_fwd_diag_timeout(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                    const FwdArgs& a, cudaStream_t stream);
 
 // Fills O = 0 and LSE = -inf for rows that see no key at all (Nk == 0).
 cudaError_t launch_fwd_empty(const FwdArgs& a, int d_v, cudaStream_t stream);

@@ -70,10 +70,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed. Returns false
-// (and records DEV_TIMEOUT_MBAR) if it does not within kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status, uint32_t where) {
+// (and records DEV_TIMEOUT_MBAR) if it does not within `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status, uint32_t where,
+                                          uint32_t limit = kSpinLimit) {
   if (mbar_try_wait(bar, parity)) return true;
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;  // try_wait itself suspends for a while
     // Back off only after ~1M polls: sleeping earlier delays the hand-offs on
     // the critical path (a woken MMA thread is hundreds of cycles late).
@@ -90,8 +91,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 // mbar_wait for code that all 32 lanes of a warp run together and that issues
 // warp-collective instructions (tcgen05.ld/st, votes) afterwards: if any lane's
 // wait failed, every lane sees false, so the warp leaves its loop as one.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status, uint32_t where) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, where));
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status, uint32_t where,
+                                               uint32_t limit = kSpinLimit) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, where, limit));
 }
 
 // ---------------------------------------------------------------------------

@@ -47,6 +47,11 @@
  * per-process device status word, read (and cleared) by
  * attn_get_device_status. All entry points are thread-safe for distinct
  * output buffers.
+ *
+ * Devices. Each call runs on the device that owns its tensors: it makes that
+ * device current on the calling thread for the duration of the call and then
+ * restores the thread's previous current device (when that device's context
+ * already exists; the call never creates a context on another GPU).
  */
 #ifndef ATTN_GB300_H_
 #define ATTN_GB300_H_
@@ -160,8 +165,9 @@ attn_status_t attn_fwd(const attn_fwd_params* p, void* workspace, size_t workspa
  * max_kv]) are device arrays owned by the caller, shared by every (batch,
  * head), 4-byte aligned; ceil(seqlen_q / 256) * max_kv < 2^31. Counts are
  * clamped to [0, max_kv]; indices outside [0, ceil(seqlen_k / 128)) list
- * nothing; a block listed twice for one query block is counted twice (the
- * caller lists each at most once). Rows that see no key get O = 0,
+ * nothing. Each key block must be listed at most once per query block: the
+ * forward counts a repeated block once per listing, and the backward's result
+ * for repeated blocks is undefined. Rows that see no key get O = 0,
  * LSE = -inf. Bad arguments give ATTN_ERR_INVALID_ARG before any launch.
  * The gradients come from attn_bwd_block_sparse. */
 attn_status_t attn_fwd_block_sparse(const attn_fwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
@@ -176,7 +182,8 @@ attn_status_t attn_bwd_varlen(const attn_bwd_params* p, void* workspace, size_t 
                               attn_stream_t stream);
 
 /* Block-sparse backward: the gradients of attn_fwd_block_sparse for the same
- * kv_count / kv_index / max_kv (same rules; dense layout only). The key
+ * kv_count / kv_index / max_kv (same rules, blocks listed at most once;
+ * dense layout only). The lists must be on the same GPU as q. The key
  * blocks' transposed lists are built on the stream into the workspace, whose
  * size is attn_bwd_block_sparse_workspace_size(p) (16-byte aligned). Both
  * modes are bitwise reproducible, as for attn_bwd. */
@@ -208,6 +215,18 @@ attn_status_t attn_bwd_noalloc(const attn_bwd_params* p, attn_stream_t stream);
  * forward kernel's softmax uses (wittx "FlashAttention-4", section
  * 用软件"伪造"硬件指令). */
 attn_status_t attn_exp2_eval(const float* x, float* y_poly, float* y_hw, int64_t n, attn_stream_t stream);
+
+/* Diagnostic for the failure path of the bounded waits: launches the dense
+ * forward kernel (d_qk = d_v = 64, exp2_emu_period 0, seqlen_q, seqlen_k >= 1,
+ * other rules as attn_fwd) in a mode where its loader issues no copies and
+ * every wait gives up after spin_limit polls (1 <= spin_limit <= 2^20). The
+ * MMA and softmax waits then run out: the kernel records ATTN_ERR_TIMEOUT in
+ * the device status word (code 1 << 24 | the site of the first wait that gave
+ * up), leaves O and LSE unspecified, and returns with no copy or MMA in
+ * flight, so the context stays usable. Read the outcome with
+ * attn_get_device_status. Not part of the computation; it exists to test
+ * that a wait that runs out is reported instead of hanging. */
+attn_status_t attn_diag_wait_timeout(const attn_fwd_params* p, uint32_t spin_limit, attn_stream_t stream);
 
 /* Synchronises `stream`, then returns ATTN_OK if no kernel recorded a
  * failure since the last call, else ATTN_ERR_TIMEOUT (the word is cleared).

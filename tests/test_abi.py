@@ -182,3 +182,39 @@ def test_header_compiles_as_c_and_cpp(lang, std):
     r = subprocess.run([cc, "-x", lang, std, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-I", inc, "-"],
                        input=src, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+@pytest.mark.parametrize("mutate,limit", [
+    (lambda p: None, 0),                                     # no poll limit
+    (lambda p: None, (1 << 20) + 1),                         # limit above 2^20
+    (lambda p: (setattr(p, "d_qk", 128), setattr(p, "d_v", 128)), 1024),  # built for d = 64 only
+    (lambda p: setattr(p, "exp2_emu_period", 8), 1024),
+    (lambda p: setattr(p, "seqlen_k", 0), 1024),            # the kernel would not launch
+    (lambda p: setattr(p, "cu_seqlens_q", 0x10000), 1024),  # dense layout only
+])
+def test_diag_wait_timeout_rejects_bad_arguments_without_a_gpu(lib, _abi, mutate, limit):
+    p = _valid_fwd(_abi)
+    mutate(p)
+    assert lib.attn_diag_wait_timeout(ctypes.byref(p), limit, None) == _abi.ATTN_ERR_INVALID_ARG
+
+
+def test_bwd_workspace_size_is_zero_for_negative_shapes(lib, _abi):
+    p = _abi.AttnBwdParams()
+    p.fwd = _valid_fwd(_abi)
+    assert lib.attn_bwd_workspace_size(ctypes.byref(p)) >= 4 * 4 * 128
+    for field, value in (("seqlen_q", -1), ("heads", -3), ("batch", -2)):
+        p.fwd = _valid_fwd(_abi)
+        setattr(p.fwd, field, value)
+        assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == 0, field
+
+
+@pytest.mark.parametrize("field,value", [("seqlen_q", -1), ("heads", -3), ("heads", 0), ("batch", -2),
+                                         ("seqlen_k", -5)])
+def test_noalloc_rejects_negative_shapes_as_invalid(lib, _abi, field, value):
+    """A negative size is a bad argument (ATTN_ERR_INVALID_ARG), not a problem
+    too large for the fixed scratch (ATTN_ERR_WORKSPACE); checked before any
+    device call."""
+    p = _abi.AttnBwdParams()
+    p.fwd = _valid_fwd(_abi)
+    setattr(p.fwd, field, value)
+    assert lib.attn_bwd_noalloc(ctypes.byref(p), None) == _abi.ATTN_ERR_INVALID_ARG

@@ -58,10 +58,16 @@ def test_small_shapes_full(ea, dims, causal, nq, nk):
 
 
 def test_bwd_training_shape_sampled_and_deterministic(ea):
+    """B2 H16 N16384 causal: the deterministic mode gives bit-identical
+    gradients over 10 runs, and those gradients (not only the other mode's)
+    match the oracle on sampled (batch, head) pairs. The non-deterministic mode
+    is checked against the oracle as well, and, since both modes run the same
+    kernels with no cross-CTA reduction, it must equal the deterministic result
+    bit for bit."""
     w = workloads.bwd_d128_N16384()
     t = workloads.make_dense(w, device="cuda")
     o, lse = ea.attn_fwd(t["q"], t["k"], t["v"], causal=True, softmax_scale=w.scale)
-    grads = None
+    runs = {}
     for det in (True, False):
         first = None
         for rep in range(10 if det else 2):
@@ -69,12 +75,16 @@ def test_bwd_training_shape_sampled_and_deterministic(ea):
                             deterministic=det)
             if first is None:
                 first = [x.clone() for x in g]
-            else:
+            elif det:
                 for a, b in zip(first, g):
-                    assert torch.equal(a, b), "backward is not bitwise reproducible"
-        grads = first
+                    assert torch.equal(a, b), "deterministic backward is not bitwise reproducible"
+        runs[det] = first
     ea.attn_get_device_status()
-    check_pairs(t, w, *grads, workloads.sample_pairs(w.batch, w.heads, 2, seed=16384))
+    pairs = workloads.sample_pairs(w.batch, w.heads, 2, seed=16384)
+    check_pairs(t, w, *runs[True], pairs)
+    check_pairs(t, w, *runs[False], pairs)
+    for a, b in zip(runs[True], runs[False]):
+        assert torch.equal(a, b), "the two modes share their kernels and must agree bitwise"
 
 
 def test_mla_192_128_sampled(ea):
