@@ -281,6 +281,16 @@ def measure_configs(ea, dev, stream) -> dict:
             r = dense(w, bwd=False, emu=emu)
             rec(f"dense_d128_B4_N8192_{'causal' if causal else 'noncausal'}_exp2_emu_1_in_{emu}", w, r["fwd"],
                 exp2_emu_period=emu)
+    for causal in (False, True):  # the two-SM (cta_group::2) dK/dV kernel on the headline shape
+        w = workloads.dense_d128(8192, causal)
+        t = workloads.make_dense(w, device=dev)
+        o, lse = ea.attn_fwd(t["q"], t["k"], t["v"], causal=causal, softmax_scale=w.scale)
+        g = tuple(torch.empty_like(t[n]) for n in ("q", "k", "v"))
+        b = time_ms(lambda: ea.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=causal, softmax_scale=w.scale,
+                                        dq=g[0], dk=g[1], dv=g[2], cta_pair=True), stream)
+        rec(f"dense_d128_B4_N8192_{'causal' if causal else 'noncausal'}_bwd_cta_pair", w, None, b, cta_pair=True)
+        del t, o, lse, g
+        torch.cuda.empty_cache()
     w = workloads.mla_192_128()
     r = dense(w)
     rec("mla_192_128_B2_H32_N8192_causal", w, r["fwd"], r[False])

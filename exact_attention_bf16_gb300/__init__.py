@@ -168,8 +168,9 @@ def attn_fwd_block_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_
     p = AttnFwdParams()
     _fill_fwd(p, q, k, v, out, lse, _strides4, scale, causal)
     p.batch, p.seqlen_q, p.seqlen_k = B, Nq, Nk
+    ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_fwd_block_sparse(ctypes.byref(p), _ptr(kv_count), _ptr(kv_index), int(kv_index.shape[1]),
-                                          _stream(stream)), "attn_fwd_block_sparse")
+                                          _ptr(ws), nbytes, _stream(stream)), "attn_fwd_block_sparse")
     return out, lse
 
 
@@ -206,13 +207,14 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
     return out, lse
 
 
-def _fill_bwd(p: AttnBwdParams, do, dq, dk, dv, strides, deterministic):
+def _fill_bwd(p: AttnBwdParams, do, dq, dk, dv, strides, deterministic, cta_pair=False):
     p.dout, p.dq, p.dk, p.dv = _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv)
     (p.do_batch_stride, p.do_row_stride, p.do_head_stride) = strides(do)
     (p.dq_batch_stride, p.dq_row_stride, p.dq_head_stride) = strides(dq)
     (p.dk_batch_stride, p.dk_row_stride, p.dk_head_stride) = strides(dk)
     (p.dv_batch_stride, p.dv_row_stride, p.dv_head_stride) = strides(dv)
     p.deterministic = 1 if deterministic else 0
+    p.cta_pair = 1 if cta_pair else 0
 
 
 def _event_handles(events):
@@ -230,9 +232,11 @@ def _event_handles(events):
 
 
 def attn_bwd(q, k, v, out, lse, dout, *, causal: bool = False, softmax_scale: Optional[float] = None,
-             deterministic: bool = False, dq=None, dk=None, dv=None, stream=None, phase_events=None):
+             deterministic: bool = False, dq=None, dk=None, dv=None, stream=None, phase_events=None,
+             cta_pair: bool = False):
     """Dense backward: returns (dQ, dK, dV) bf16 for the loss <O, dO>. ``phase_events`` (optional, three
-    torch.cuda.Event) are recorded after the D pass, the dK/dV kernel and the dQ kernel."""
+    torch.cuda.Event) are recorded after the D pass, the dK/dV kernel and the dQ kernel. ``cta_pair``
+    selects the two-SM (cta_group::2) dK/dV kernel (d = 128)."""
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
         _check_bf16(n, t, 4)
     B, Nq, H, dqk = q.shape
@@ -244,7 +248,7 @@ def attn_bwd(q, k, v, out, lse, dout, *, causal: bool = False, softmax_scale: Op
     p = AttnBwdParams()
     _fill_fwd(p.fwd, q, k, v, out, lse, _strides4, scale, causal)
     p.fwd.batch, p.fwd.seqlen_q, p.fwd.seqlen_k = B, Nq, Nk
-    _fill_bwd(p, dout, dq, dk, dv, _strides4, deterministic)
+    _fill_bwd(p, dout, dq, dk, dv, _strides4, deterministic, cta_pair)
     handles = _event_handles(phase_events)
     if handles is not None:
         for i, h in enumerate(handles):
@@ -283,7 +287,7 @@ def attn_bwd_block_sparse(q, k, v, out, lse, dout, kv_count, kv_index, *, causal
 
 def attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int, *,
                     causal: bool = False, softmax_scale: Optional[float] = None, deterministic: bool = False,
-                    dq=None, dk=None, dv=None, stream=None):
+                    dq=None, dk=None, dv=None, stream=None, cta_pair: bool = False):
     """Packed variable-length backward: returns (dQ, dK, dV) packed like q, k, v."""
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
         _check_bf16(n, t, 3)
@@ -299,7 +303,7 @@ def attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seq
     p.fwd.max_seqlen_q, p.fwd.max_seqlen_k = int(max_seqlen_q), int(max_seqlen_k)
     p.fwd.total_q, p.fwd.total_k = tq, k.shape[0]
     p.fwd.batch = 1
-    _fill_bwd(p, dout, dq, dk, dv, _strides3, deterministic)
+    _fill_bwd(p, dout, dq, dk, dv, _strides3, deterministic, cta_pair)
     ws, nbytes = _workspace(_lib.attn_bwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_bwd_varlen(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_bwd_varlen")
     return dq, dk, dv

@@ -10,7 +10,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libattn_gb300.so")
 HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "attn.h")
 
-ABI_VERSION = 1
+ABI_VERSION = 2
 BWD_NOALLOC_SCRATCH_BYTES = 8 << 20  # ATTN_BWD_NOALLOC_SCRATCH_BYTES
 
 STATUS = {
@@ -51,7 +51,7 @@ class AttnBwdParams(ctypes.Structure):
         ("dq_batch_stride", c_i64), ("dq_row_stride", c_i64), ("dq_head_stride", c_i64),
         ("dk_batch_stride", c_i64), ("dk_row_stride", c_i64), ("dk_head_stride", c_i64),
         ("dv_batch_stride", c_i64), ("dv_row_stride", c_i64), ("dv_head_stride", c_i64),
-        ("deterministic", c_i32), ("reserved0", c_i32),
+        ("deterministic", c_i32), ("cta_pair", c_i32),
         ("phase_events", c_vp * 3),
     ]
 
@@ -75,7 +75,8 @@ def load(path: str = LIB_PATH):
         "attn_bwd_workspace_size": (ctypes.c_size_t, [P(AttnBwdParams)]),
         "attn_fwd": (ctypes.c_int, [P(AttnFwdParams), c_vp, ctypes.c_size_t, c_vp]),
         "attn_fwd_varlen": (ctypes.c_int, [P(AttnFwdParams), c_vp, ctypes.c_size_t, c_vp]),
-        "attn_fwd_block_sparse": (ctypes.c_int, [P(AttnFwdParams), c_vp, c_vp, ctypes.c_int32, c_vp]),
+        "attn_fwd_block_sparse": (ctypes.c_int, [P(AttnFwdParams), c_vp, c_vp, ctypes.c_int32, c_vp, ctypes.c_size_t,
+                                                 c_vp]),
         "attn_bwd_block_sparse_workspace_size": (ctypes.c_size_t, [P(AttnBwdParams)]),
         "attn_bwd_block_sparse": (ctypes.c_int, [P(AttnBwdParams), c_vp, c_vp, ctypes.c_int32, c_vp,
                                                  ctypes.c_size_t, c_vp]),

@@ -106,10 +106,11 @@ cudaError_t DeviceScope::bind(const void* ptr) {
   e = cudaGetDevice(&prev_);
   if (e != cudaSuccess) return e;
   device_ = attr.device;
-  if (prev_ == device_) return cudaSuccess;
-  // cudaSetDevice also makes the device's primary context current on this thread.
+  // Always select it: cudaSetDevice also makes the device's primary context
+  // current on this thread, which a thread that never used the runtime (an
+  // autograd worker) lacks even when its default device is the right one.
   e = cudaSetDevice(device_);
-  if (e == cudaSuccess) switched_ = true;
+  if (e == cudaSuccess && prev_ != device_) switched_ = true;
   return e;
 }
 
@@ -222,9 +223,22 @@ struct SparseSpec {
   int32_t max_kv = 0;
 };
 
+// Forward workspace: a 256-byte block holding the range flag, then the fp16
+// copy of V ([rows, heads, d_v], contiguous) that the PV product reads.
+size_t fwd_v16_bytes(const attn_fwd_params* p, bool varlen) {
+  if (p->heads < 1 || p->d_v <= 0) return 0;
+  const int64_t rows = varlen ? static_cast<int64_t>(p->total_k) : static_cast<int64_t>(p->batch) * p->seqlen_k;
+  if (rows <= 0) return 0;
+  return static_cast<size_t>((rows * p->heads * p->d_v * 2 + 255) / 256 * 256);
+}
+size_t fwd_workspace_bytes(const attn_fwd_params* p, bool varlen) {
+  const size_t v16 = fwd_v16_bytes(p, varlen);
+  return v16 ? 256 + v16 : 0;
+}
+
 // diag_limit != 0: the diagnostic launch of attn_diag_wait_timeout instead of the forward.
-attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream, const SparseSpec& sp = {},
-                      uint32_t diag_limit = 0) {
+attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream, void* ws, size_t ws_bytes,
+                      const SparseSpec& sp = {}, uint32_t diag_limit = 0) {
   ATTN_TRY(check_fwd(p, varlen));
   if (p->exp2_emu_period != 0 && p->exp2_emu_period != 4 && p->exp2_emu_period != 8) return ATTN_ERR_INVALID_ARG;
   const int nq_rows = varlen ? p->total_q : p->seqlen_q;
@@ -232,6 +246,9 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
   const int units = varlen ? p->num_seqs : p->batch;
   const int max_q = varlen ? p->max_seqlen_q : p->seqlen_q;
   if (nq_rows == 0 || max_q == 0) return ATTN_OK;
+  const size_t need_ws = diag_limit ? 0 : fwd_workspace_bytes(p, varlen);
+  if (nk_rows > 0 && need_ws > 0 && (ws == nullptr || ws_bytes < need_ws || (reinterpret_cast<uintptr_t>(ws) & 255u)))
+    return ATTN_ERR_WORKSPACE;
   DeviceScope scope;
   {
     cudaError_t be = scope.bind(p->q ? p->q : p->k);
@@ -285,9 +302,25 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
                     p->k_head_stride, 128));
   ATTN_TRY(make_map(&tv, p->v, p->d_v, p->heads, nk_rows, nb, p->v_batch_stride, p->v_row_stride,
                     p->v_head_stride, 128));
-  e = diag_limit ? launch_fwd_diag_timeout(tq, tk, tv, a, stream)
-      : sp.kv_count ? launch_fwd_sparse(p->d_qk, p->d_v, tq, tk, tv, a, stream)
-                    : launch_fwd(p->d_qk, p->d_v, tq, tk, tv, a, stream);
+  if (diag_limit) {
+    e = launch_fwd_diag_timeout(tq, tk, tv, a, stream);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "fwd diag launch");
+  }
+  // fp16 copy of V for the PV product, and its range flag
+  uint32_t* flag = static_cast<uint32_t*>(ws);
+  void* v16 = static_cast<uint8_t*>(ws) + 256;
+  const int64_t v16_rows = varlen ? p->total_k : p->seqlen_k;
+  CUtensorMap tv16;
+  ATTN_TRY(make_map(&tv16, v16, p->d_v, p->heads, nk_rows, nb, v16_rows * p->heads * p->d_v,
+                    static_cast<int64_t>(p->heads) * p->d_v, p->d_v, 128));
+  e = cudaMemsetAsync(flag, 0, sizeof(uint32_t), stream);
+  if (e == cudaSuccess)
+    e = launch_v_to_f16(p->v, varlen ? 0 : p->v_batch_stride, p->v_row_stride, p->v_head_stride, nb, nk_rows,
+                        p->heads, p->d_v, v16, flag, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fwd V conversion");
+  a.v16_flag = flag;
+  e = sp.kv_count ? launch_fwd_sparse(p->d_qk, p->d_v, tq, tk, tv, tv16, a, stream)
+                  : launch_fwd(p->d_qk, p->d_v, tq, tk, tv, tv16, a, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "fwd launch");
 }
 
@@ -321,6 +354,7 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
   ATTN_TRY(check_tensor(p->dq, p->dq_batch_stride, p->dq_row_stride, p->dq_head_stride, varlen, eq));
   ATTN_TRY(check_tensor(p->dk, p->dk_batch_stride, p->dk_row_stride, p->dk_head_stride, varlen, ek));
   ATTN_TRY(check_tensor(p->dv, p->dv_batch_stride, p->dv_row_stride, p->dv_head_stride, varlen, ek));
+  if (p->cta_pair && (f.d_qk != 128 || f.d_v != 128 || sp.kv_count)) return ATTN_ERR_UNSUPPORTED;
   const int nq_rows = varlen ? f.total_q : f.seqlen_q;
   const int nk_rows = varlen ? f.total_k : f.seqlen_k;
   if (nq_rows == 0 && nk_rows == 0) return ATTN_OK;
@@ -402,7 +436,16 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
   if (e == cudaSuccess && sp.kv_count) e = launch_bwd_transpose_lists(a, n_kb_sparse, stream);
   if (e == cudaSuccess) e = mark(0);
   if (e != cudaSuccess) return cuda_fail(e, "bwd preprocess launch");
-  e = launch_bwd_dkdv(f.d_qk, f.d_v, tq2, tk, tv, tdo2, a, stream);
+  if (p->cta_pair) {  // the two-SM kernel (d = 128, no block lists; checked before any launch)
+    CUtensorMap tq_r, tdo_r;
+    ATTN_TRY(make_map(&tq_r, f.q, f.d_qk, f.heads, nq_rows, nb, f.q_batch_stride, f.q_row_stride, f.q_head_stride,
+                      64));
+    ATTN_TRY(make_map(&tdo_r, p->dout, f.d_v, f.heads, nq_rows, nb, p->do_batch_stride, p->do_row_stride,
+                      p->do_head_stride, 64));
+    e = launch_bwd_dkdv_pair(tq_r, tq2, tk, tv, tdo_r, tdo2, a, stream);
+  } else {
+    e = launch_bwd_dkdv(f.d_qk, f.d_v, tq2, tk, tv, tdo2, a, stream);
+  }
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return cuda_fail(e, "bwd dkdv launch");
   e = launch_bwd_dq(f.d_qk, f.d_v, tq, tk, tv, tdo, a, stream);
@@ -419,25 +462,21 @@ using namespace gb300;
 extern "C" {
 
 size_t attn_fwd_workspace_size(const attn_fwd_params* p) {
-  (void)p;
-  return 0;
+  if (!p) return 0;
+  return fwd_workspace_bytes(p, p->cu_seqlens_q != nullptr);
 }
 
 attn_status_t attn_fwd(const attn_fwd_params* p, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
-  return run_fwd(p, false, static_cast<cudaStream_t>(stream));
+  return run_fwd(p, false, static_cast<cudaStream_t>(stream), workspace, workspace_bytes);
 }
 
 attn_status_t attn_fwd_varlen(const attn_fwd_params* p, void* workspace, size_t workspace_bytes,
                               attn_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
-  return run_fwd(p, true, static_cast<cudaStream_t>(stream));
+  return run_fwd(p, true, static_cast<cudaStream_t>(stream), workspace, workspace_bytes);
 }
 
 attn_status_t attn_fwd_block_sparse(const attn_fwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
-                                    int32_t max_kv, attn_stream_t stream) {
+                                    int32_t max_kv, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
   ATTN_TRY(check_fwd(p, false));
   if (p->exp2_emu_period != 0) return ATTN_ERR_INVALID_ARG;
   const int64_t n_qblk = (static_cast<int64_t>(p->seqlen_q) + 255) / 256;
@@ -451,7 +490,7 @@ attn_status_t attn_fwd_block_sparse(const attn_fwd_params* p, const int32_t* kv_
   sp.kv_count = kv_count;
   sp.kv_index = kv_index;
   sp.max_kv = max_kv;
-  return run_fwd(p, false, static_cast<cudaStream_t>(stream), sp);
+  return run_fwd(p, false, static_cast<cudaStream_t>(stream), workspace, workspace_bytes, sp);
 }
 
 size_t attn_bwd_block_sparse_workspace_size(const attn_bwd_params* p) {
@@ -509,7 +548,7 @@ attn_status_t attn_diag_wait_timeout(const attn_fwd_params* p, uint32_t spin_lim
   if (p->d_qk != 64 || p->d_v != 64 || p->exp2_emu_period != 0) return ATTN_ERR_INVALID_ARG;
   if (spin_limit < 1 || spin_limit > (1u << 20)) return ATTN_ERR_INVALID_ARG;
   if (p->seqlen_q == 0 || p->seqlen_k == 0) return ATTN_ERR_INVALID_ARG;  // the kernel must launch
-  return run_fwd(p, false, static_cast<cudaStream_t>(stream), SparseSpec{}, spin_limit);
+  return run_fwd(p, false, static_cast<cudaStream_t>(stream), nullptr, 0, SparseSpec{}, spin_limit);
 }
 
 attn_status_t attn_get_device_status(attn_stream_t stream, uint32_t* detail) {

@@ -20,7 +20,17 @@
 // exp2 runs on the hardware unit for most columns and on the FMA pipe
 // (exp2_emu.cuh) for a fixed 1/EMU_PERIOD of them (same page, section
 // 用软件"伪造"硬件指令).
+//
+// P enters the PV MMA in fp16 (11 significant bits) rather than bf16 (8):
+// under a stale max a row's largest weights reach 2^8 and carry their own
+// rounding, which with bf16 moves O by up to ~2e-2 on rows that concentrate on
+// a few keys. The MMA takes A and B of one type, so V is read from an fp16 copy
+// made by v_to_f16_kernel before the launch (exact for |v| < 65536). When that
+// pass found a finite value outside fp16's range (a.v16_flag != 0), or no copy
+// was made (a.v16_flag == nullptr), V and P stay bf16 for the whole call.
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "exp2_emu.cuh"
 #include "kernels.h"
@@ -74,6 +84,9 @@ struct Bars {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// V (and so P) in fp16 for this call: a copy was made and every value fit.
+__device__ __forceinline__ bool v_is_f16(const FwdArgs& a) { return a.v16_flag != nullptr && __ldg(a.v16_flag) == 0u; }
+
 // Number of visible keys of query row `row` (0-based within its sequence).
 __device__ __forceinline__ int key_limit(int row, int nq, int nk, int causal) {
   if (!causal) return nk;
@@ -93,7 +106,8 @@ __device__ __forceinline__ int key_limit(int row, int nq, int nk, int causal) {
 template <int DQK, int DV, int EMU_PERIOD, bool SPARSE = false, bool DIAG = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmv, const FwdArgs a) {
+                    const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmv16,
+                    const FwdArgs a) {
   using C = Cfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -185,12 +199,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && !DIAG) {
       tma_prefetch_desc(&tmq);
       tma_prefetch_desc(&tmk);
-      tma_prefetch_desc(&tmv);
       for (int i = 0; i < QT; ++i) {
         mbar_arrive_expect_tx(&bar->q_full[i], C::Q_BYTES);
         for (int c = 0; c < C::QCH; ++c)
           tma_load_4d(sQ + i * C::Q_BYTES + c * kChunk, &tmq, &bar->q_full[i], c * 64, h, q_start + row0 + i * BM, b);
       }
+      // read while the Q copies fly: V from the fp16 copy, or the bf16 original
+      const CUtensorMap* tmvv = v_is_f16(a) ? &tmv16 : &tmv;
+      tma_prefetch_desc(tmvv);
       int issued = 0;
       bool ok = true;
       for (int j = 0; j < nkv_max && ok; ++j) {
@@ -209,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             mbar_arrive_expect_tx(&bar->kv_full[slot], C::V_BYTES);
             for (int c = 0; c < C::VCH; ++c)
-              tma_load_4d(dst + c * kChunk, &tmv, &bar->kv_full[slot], c * 64, h, k_start + kb * BN, b);
+              tma_load_4d(dst + c * kChunk, tmvv, &bar->kv_full[slot], c * 64, h, k_start + kb * BN, b);
           }
           ++issued;
         }
@@ -226,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================= MMA issuer =====================================
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
-      constexpr uint32_t idO = idesc_bf16_f32(BM, DV, false, true);
+      const uint32_t idO = v_is_f16(a) ? idesc_f16_f32(BM, DV, false, true) : idesc_bf16_f32(BM, DV, false, true);
       bool ok = mbar_wait(&bar->q_full[0], 0, a.status, 0x200, lim) &&
                 mbar_wait(&bar->q_full[1], 0, a.status, 0x201, lim);
       for (int j = 0; j <= nkv_max && ok; ++j) {
@@ -287,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lim = key_limit(row, nq, nk, a.causal);
     const uint32_t lane_base = tbase + ((quarter * 32u) << 16);
     const float sl2 = a.scale_log2;
+    const bool f16 = v_is_f16(a);  // P packed as fp16 (V's copy) or bf16
     float m_used = -INFINITY;  // log2 units
     float l = 0.f;  // row sum of the fp32 weights
     int n_rescale = 0, n_opp = 0;
@@ -330,26 +347,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l *= alpha;
       const float mu = (m_used == -INFINITY) ? 0.f : m_used;
-      // p = 2^(s * scale * log2e - m_used), packed to bf16 pairs in place
+      // p = 2^(s * scale * log2e - m_used), packed to fp16 (or bf16) pairs in place
       uint32_t pk[BN / 2];
       float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // partial row sums (packed pairs)
       const float2 sl2v = make_float2(sl2, sl2), negmu = make_float2(-mu, -mu);
+      auto exp_row = [&](auto f16_tag) {
+        constexpr bool F16 = decltype(f16_tag)::value;
 #pragma unroll
-      for (int c = 0; c < BN / 2; ++c) {
-        const float2 x = ffma2(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sl2v, negmu);
-        float2 p;
-        if constexpr (EMU_PERIOD > 0) {
-          if (((2 * c) % EMU_PERIOD) == EMU_PERIOD - 2) {
-            p = make_float2(ex2_mufu(x.x), ex2_emu(x.y));
+        for (int c = 0; c < BN / 2; ++c) {
+          const float2 x = ffma2(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sl2v, negmu);
+          float2 p;
+          if constexpr (EMU_PERIOD > 0) {
+            if (((2 * c) % EMU_PERIOD) == EMU_PERIOD - 2) {
+              p = make_float2(ex2_mufu(x.x), ex2_emu(x.y));
+            } else {
+              p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+            }
           } else {
             p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
           }
-        } else {
-          p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+          pk[c] = F16 ? pack_f16x2(p.x, p.y) : pack_bf16x2(p.x, p.y);
+          rs[c & 1] = fadd2(rs[c & 1], p);
         }
-        pk[c] = pack_bf16x2(p.x, p.y);
-        rs[c & 1] = fadd2(rs[c & 1], p);
-      }
+      };
+      if (f16) exp_row(std::true_type{});
+      else exp_row(std::false_type{});
       l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
       tmem_st32(lane_base + tS(i) + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st32(lane_base + tS(i) + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
@@ -443,8 +465,8 @@ __global__ void exp2_eval_kernel(const float* x, float* yp, float* yh, int64_t n
 }
 
 template <int DQK, int DV, int EMU, bool SPARSE = false, bool DIAG = false>
-cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
-                     cudaStream_t stream) {
+cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tv16,
+                     const FwdArgs& a, cudaStream_t stream) {
   using C = Cfg<DQK, DV>;
   auto kern = attn_fwd_kernel<DQK, DV, EMU, SPARSE, DIAG>;
   static PerDeviceOnce once;
@@ -461,47 +483,89 @@ cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   const int64_t grid = static_cast<int64_t>(a.n_mblk) * a.num_units * a.heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM, stream>>>(tq, tk, tv, a);
+  kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM, stream>>>(tq, tk, tv, tv16, a);
   return cudaGetLastError();
 }
 
 // exp2 split: every EMU-th column of a row goes to the FMA-pipe polynomial
 // (0 = all on the hardware unit). Built for 0, 4 and 8.
 template <int DQK, int DV>
-cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
-                     cudaStream_t stream) {
+cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tv16,
+                     const FwdArgs& a, cudaStream_t stream) {
   switch (a.emu_period) {
-    case 0: return launch_e<DQK, DV, 0>(tq, tk, tv, a, stream);
-    case 4: return launch_e<DQK, DV, 4>(tq, tk, tv, a, stream);
-    case 8: return launch_e<DQK, DV, 8>(tq, tk, tv, a, stream);
+    case 0: return launch_e<DQK, DV, 0>(tq, tk, tv, tv16, a, stream);
+    case 4: return launch_e<DQK, DV, 4>(tq, tk, tv, tv16, a, stream);
+    case 8: return launch_e<DQK, DV, 8>(tq, tk, tv, tv16, a, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// V -> fp16 copy for the PV product (contiguous [rows, heads, d_v], rows = B * N
+// dense or total varlen). One 16-byte unit of 8 values per thread and step.
+// Sets *flag when a finite value lies outside fp16's range (|v| >= 65536,
+// which would become inf); inf and NaN convert to themselves.
+__global__ void v_to_f16_kernel(const void* v, int64_t sb, int64_t sn, int64_t sh, int nb, int nrows, int heads,
+                                int dv, void* out, uint32_t* flag) {
+  const int upr = dv / 8;  // 16-byte units per (row, head)
+  const int64_t units = static_cast<int64_t>(nb) * nrows * heads * upr;
+  uint32_t bad = 0;
+  for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
+       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int part = static_cast<int>(u % upr);
+    const int64_t rh = u / upr;  // (b, row, head), head fastest
+    const int h = static_cast<int>(rh % heads);
+    const int64_t br = rh / heads;
+    const int r = static_cast<int>(br % nrows), b = static_cast<int>(br / nrows);
+    const uint4 x = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(v) + b * sb + r * sn + h * sh +
+                                                    8 * part);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t lo = w[e] & 0x7FFFu, hi = (w[e] >> 16) & 0x7FFFu;
+      bad |= static_cast<uint32_t>(lo >= 0x4780u && lo < 0x7F80u) | static_cast<uint32_t>(hi >= 0x4780u && hi < 0x7F80u);
+      o[e] = pack_f16x2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+    }
+    reinterpret_cast<uint4*>(out)[u] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (__any_sync(0xffffffffu, bad != 0) && (threadIdx.x & 31u) == 0) atomicOr(flag, 1u);
 }
 
 }  // namespace fwd
 
 cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdArgs& a, cudaStream_t stream) {
-  if (d_qk == 64 && d_v == 64) return fwd::launch_t<64, 64>(tq, tk, tv, a, stream);
-  if (d_qk == 128 && d_v == 128) return fwd::launch_t<128, 128>(tq, tk, tv, a, stream);
-  if (d_qk == 192 && d_v == 128) return fwd::launch_t<192, 128>(tq, tk, tv, a, stream);
+                       const CUtensorMap& tv16, const FwdArgs& a, cudaStream_t stream) {
+  if (d_qk == 64 && d_v == 64) return fwd::launch_t<64, 64>(tq, tk, tv, tv16, a, stream);
+  if (d_qk == 128 && d_v == 128) return fwd::launch_t<128, 128>(tq, tk, tv, tv16, a, stream);
+  if (d_qk == 192 && d_v == 128) return fwd::launch_t<192, 128>(tq, tk, tv, tv16, a, stream);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_fwd_sparse(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const FwdArgs& a, cudaStream_t stream) {
+                              const CUtensorMap& tv16, const FwdArgs& a, cudaStream_t stream) {
   if (a.cu_q != nullptr || a.emu_period != 0 || a.kv_count == nullptr || a.max_kv < 0) return cudaErrorInvalidValue;
   if (a.max_kv > 0 && a.kv_index == nullptr) return cudaErrorInvalidValue;
-  if (d_qk == 64 && d_v == 64) return fwd::launch_e<64, 64, 0, true>(tq, tk, tv, a, stream);
-  if (d_qk == 128 && d_v == 128) return fwd::launch_e<128, 128, 0, true>(tq, tk, tv, a, stream);
-  if (d_qk == 192 && d_v == 128) return fwd::launch_e<192, 128, 0, true>(tq, tk, tv, a, stream);
+  if (d_qk == 64 && d_v == 64) return fwd::launch_e<64, 64, 0, true>(tq, tk, tv, tv16, a, stream);
+  if (d_qk == 128 && d_v == 128) return fwd::launch_e<128, 128, 0, true>(tq, tk, tv, tv16, a, stream);
+  if (d_qk == 192 && d_v == 128) return fwd::launch_e<192, 128, 0, true>(tq, tk, tv, tv16, a, stream);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_fwd_diag_timeout(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const FwdArgs& a, cudaStream_t stream) {
-  if (a.cu_q != nullptr || a.kv_count != nullptr || a.spin_limit == 0) return cudaErrorInvalidValue;
-  return fwd::launch_e<64, 64, 0, false, true>(tq, tk, tv, a, stream);
+  if (a.cu_q != nullptr || a.kv_count != nullptr || a.spin_limit == 0 || a.v16_flag != nullptr)
+    return cudaErrorInvalidValue;
+  return fwd::launch_e<64, 64, 0, false, true>(tq, tk, tv, tv, a, stream);
+}
+
+cudaError_t launch_v_to_f16(const void* v, int64_t sb, int64_t sn, int64_t sh, int nb, int nrows, int heads, int dv,
+                            void* out, uint32_t* flag, cudaStream_t stream) {
+  const int64_t units = static_cast<int64_t>(nb) * nrows * heads * (dv / 8);
+  if (units == 0) return cudaSuccess;
+  const int64_t blocks = (units + 255) / 256 < 152 * 16 ? (units + 255) / 256 : 152 * 16;
+  fwd::v_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(v, sb, sn, sh, nb, nrows, heads, dv, out,
+                                                                         flag);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_empty(const FwdArgs& a, int d_v, cudaStream_t stream) {

@@ -1,0 +1,42 @@
+// Pieces shared by the backward kernels (attn_bwd.cu, attn_bwd_pair.cu):
+// tile sizes, warp roles, row stores and the bounds of a work unit.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+
+namespace gb300 {
+namespace bwd {
+
+constexpr int KB = 128;          // keys per kv tile (TMEM lanes in dkdv)
+constexpr int MB = 128;          // queries per q tile in the dq kernel
+constexpr int kThreads = 320;    // 8 softmax warps + TMA warp + MMA warp
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kSoftThreads = 256;
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&w)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) d[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+}
+
+// Sequence bounds of a work unit (dense: unit = batch index).
+struct Unit {
+  int b, q_start, k_start, nq, nk;
+};
+__device__ __forceinline__ Unit unit_bounds(const BwdArgs& a, int unit) {
+  Unit u{unit, 0, 0, a.seqlen_q, a.seqlen_k};
+  if (a.cu_q != nullptr) {
+    u.b = 0;
+    u.q_start = a.cu_q[unit];
+    u.nq = a.cu_q[unit + 1] - u.q_start;
+    u.k_start = a.cu_k[unit];
+    u.nk = a.cu_k[unit + 1] - u.k_start;
+  }
+  return u;
+}
+
+}  // namespace bwd
+}  // namespace gb300

@@ -71,15 +71,25 @@ struct FwdArgs {
   const int* kv_index;
   int max_kv;
   uint32_t spin_limit;       // diagnostic launches only: poll limit of every wait
+  // Device word written by v_to_f16 before the launch: 0 = V is read from the
+  // fp16 copy (map tv16) and P is packed in fp16; nonzero, or a null pointer,
+  // = V and P in bf16.
+  const uint32_t* v16_flag;
 };
 
 cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdArgs& a, cudaStream_t stream);
+                       const CUtensorMap& tv16, const FwdArgs& a, cudaStream_t stream);
+
+// fp16 copy of V (contiguous [nb, nrows, heads, dv]) for the forward's PV
+// product; ORs 1 into *flag (zeroed by the caller) if a finite value is out of
+// fp16's range.
+cudaError_t launch_v_to_f16(const void* v, int64_t sb, int64_t sn, int64_t sh, int nb, int nrows, int heads, int dv,
+                            void* out, uint32_t* flag, cudaStream_t stream);
 
 // Block-sparse forward (dense layout, cu_q == nullptr, emu_period == 0): the
 // same kernel walking a.kv_index's key blocks instead of 0 .. nkv-1.
 cudaError_t launch_fwd_sparse(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const FwdArgs& a, cudaStream_t stream);
+                              const CUtensorMap& tv16, const FwdArgs& a, cudaStream_t stream);
 
 // Diagnostic: the d = 64 dense forward with no copies issued and every wait
 // limited to a.spin_limit polls (attn_diag_wait_timeout).
@@ -133,6 +143,11 @@ cudaError_t launch_bwd_preprocess(int d_v, const BwdArgs& a, cudaStream_t stream
 // a.kv_count set they walk the block-sparse lists (dense layout only).
 cudaError_t launch_bwd_dkdv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+// dK, dV for d_qk = d_v = 128 over CTA pairs (dense or varlen, no block
+// lists): maps q and dO with 64-row boxes (_r) and 128-row boxes (_c), k, v.
+cudaError_t launch_bwd_dkdv_pair(const CUtensorMap& tq_r, const CUtensorMap& tq_c, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const CUtensorMap& tdo_r, const CUtensorMap& tdo_c,
+                                 const BwdArgs& a, cudaStream_t stream);
 // Builds a.q_count / a.q_index (transposed block lists) from a.kv_count / a.kv_index
 // for n_kb key blocks, deterministically (ascending query blocks).
 cudaError_t launch_bwd_transpose_lists(const BwdArgs& a, int n_kb, cudaStream_t stream);

@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 1
+#define ATTN_ABI_VERSION 2
 
 typedef enum {
   ATTN_OK = 0,
@@ -129,7 +129,17 @@ typedef struct attn_fwd_params {
  * on identical inputs give bitwise-identical dq/dk/dv on the same device. This
  * implementation reduces dQ inside one query-stationary CTA per tile (no
  * atomics, no cross-CTA reduction), so deterministic == 0 reproduces bitwise
- * too; the flag is accepted for interface compatibility. */
+ * too; the flag is accepted for interface compatibility.
+ *
+ * cta_pair != 0 computes dK, dV with the two-SM kernel (wittx
+ * "FlashAttention-4", section 反向传播的优化): a cluster of two CTAs runs one
+ * tcgen05 MMA (cta_group::2) whose accumulator is split along the keys and whose
+ * B operand is split along N, so each SM holds and reads half of every Q / dO
+ * tile. Only d_qk = d_v = 128 without block lists (else ATTN_ERR_UNSUPPORTED);
+ * the results are the same gradients within rounding, bitwise reproducible.
+ * The default (0) is the one-SM kernel, the faster of the two on GB300: one
+ * pair MMA takes ~107 cycles to issue, more than the 64 cycles of work an
+ * N = 128 instruction gives each SM. */
 typedef struct attn_bwd_params {
   attn_fwd_params fwd;
   const void* dout;
@@ -141,14 +151,22 @@ typedef struct attn_bwd_params {
   int64_t dk_batch_stride, dk_row_stride, dk_head_stride;
   int64_t dv_batch_stride, dv_row_stride, dv_head_stride;
   int32_t deterministic;
-  int32_t reserved0;
+  int32_t cta_pair;
   /* Optional (each may be NULL): CUDA events (cudaEvent_t) recorded on the
    * stream after the D = rowsum(dO * O) pass [0], after the dK/dV kernel [1]
    * and after the dQ kernel [2], for timing the phases. */
   void* phase_events[3];
 } attn_bwd_params;
 
-/* Bytes of device workspace the matching call needs (0 means none: pass NULL). */
+/* Bytes of device workspace the matching call needs (0 means none: pass NULL).
+ * The forward's workspace (also for attn_fwd_varlen and attn_fwd_block_sparse)
+ * holds an fp16 copy of V, made on the stream before the attention kernel: P
+ * and V enter the PV product in fp16 (11 significant bits) rather than bf16,
+ * which keeps O within 1e-2 of the exact result where a few keys dominate a
+ * row. Its size is 256 + 2 * (keys x heads x d_v) bytes, rounded up to 256;
+ * it must be 256-byte aligned. When V holds a finite value with |v| >= 65536
+ * (outside fp16's range), that call computes the PV product in bf16
+ * instead. */
 size_t attn_fwd_workspace_size(const attn_fwd_params* p);
 size_t attn_bwd_workspace_size(const attn_bwd_params* p);
 
@@ -169,9 +187,10 @@ attn_status_t attn_fwd(const attn_fwd_params* p, void* workspace, size_t workspa
  * forward counts a repeated block once per listing, and the backward's result
  * for repeated blocks is undefined. Rows that see no key get O = 0,
  * LSE = -inf. Bad arguments give ATTN_ERR_INVALID_ARG before any launch.
- * The gradients come from attn_bwd_block_sparse. */
+ * The workspace is that of attn_fwd (attn_fwd_workspace_size). The gradients
+ * come from attn_bwd_block_sparse. */
 attn_status_t attn_fwd_block_sparse(const attn_fwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
-                                    int32_t max_kv, attn_stream_t stream);
+                                    int32_t max_kv, void* workspace, size_t workspace_bytes, attn_stream_t stream);
 /* Variable-length forward (cu_seqlens_q / cu_seqlens_k required). */
 attn_status_t attn_fwd_varlen(const attn_fwd_params* p, void* workspace, size_t workspace_bytes,
                               attn_stream_t stream);

@@ -141,7 +141,7 @@ def test_block_sparse_rejects_bad_arguments_without_a_gpu(lib, _abi, mutate, exp
     p = _valid_fwd(_abi)
     p.seqlen_q = 600  # three query blocks of 256 rows
     p, (cnt, idx, max_kv) = mutate(p, _valid_sparse_args())
-    assert lib.attn_fwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, None) == expect
+    assert lib.attn_fwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, None, 0, None) == expect
 
 
 @pytest.mark.parametrize("mutate,expect", [
@@ -218,3 +218,36 @@ def test_noalloc_rejects_negative_shapes_as_invalid(lib, _abi, field, value):
     p.fwd = _valid_fwd(_abi)
     setattr(p.fwd, field, value)
     assert lib.attn_bwd_noalloc(ctypes.byref(p), None) == _abi.ATTN_ERR_INVALID_ARG
+
+
+def test_cta_pair_backward_only_for_d128_without_lists(lib, _abi):
+    """The two-SM dK/dV kernel exists for d_qk = d_v = 128 without block lists;
+    asking for it elsewhere is ATTN_ERR_UNSUPPORTED before any device call."""
+    p = _abi.AttnBwdParams()
+    p.fwd = _valid_fwd(_abi)  # d = 64
+    p.dout = p.dq = p.dk = p.dv = 0x10000
+    for t in ("do", "dq", "dk", "dv"):
+        setattr(p, f"{t}_batch_stride", 128 * 4 * 64)
+        setattr(p, f"{t}_row_stride", 4 * 64)
+        setattr(p, f"{t}_head_stride", 64)
+    p.cta_pair = 1
+    assert lib.attn_bwd(ctypes.byref(p), None, 0, None) == _abi.ATTN_ERR_UNSUPPORTED
+    p.fwd.d_qk, p.fwd.d_v = 192, 128
+    assert lib.attn_bwd(ctypes.byref(p), None, 0, None) == _abi.ATTN_ERR_UNSUPPORTED
+    p.fwd.d_qk, p.fwd.d_v = 128, 128
+    cnt, idx, max_kv = _valid_sparse_args()
+    assert lib.attn_bwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, None, 0, None) in (
+        _abi.ATTN_ERR_UNSUPPORTED, _abi.ATTN_ERR_INVALID_ARG)
+
+
+def test_fwd_workspace_size_holds_the_fp16_copy_of_v(lib, _abi):
+    p = _valid_fwd(_abi)  # B1 H4 Nk128 d_v 64
+    assert lib.attn_fwd_workspace_size(ctypes.byref(p)) == 256 + 128 * 4 * 64 * 2
+    p.seqlen_k = 0
+    assert lib.attn_fwd_workspace_size(ctypes.byref(p)) == 0
+    p.seqlen_k, p.heads = 128, -1
+    assert lib.attn_fwd_workspace_size(ctypes.byref(p)) == 0
+    p = _valid_fwd(_abi)
+    p.cu_seqlens_q = p.cu_seqlens_k = 0x10000
+    p.num_seqs, p.total_q, p.total_k, p.max_seqlen_q, p.max_seqlen_k = 2, 300, 301, 200, 200
+    assert lib.attn_fwd_workspace_size(ctypes.byref(p)) == 256 + (301 * 4 * 64 * 2 + 255) // 256 * 256

@@ -193,3 +193,38 @@ def test_exp2_paths(ea):
     # ~600x the hardware unit's error (wittx)
     ratio = rel_p.max() / rel_h.max()
     assert 100 < ratio < 5000
+
+
+@pytest.mark.parametrize("dims", [(64, 64), (128, 128), (192, 128)])
+def test_value_rows_beyond_fp16_range(dims):
+    """V tiles are converted to fp16 for the PV product; a tile holding a value
+    outside fp16's finite range (|v| >= 65536) must fall back to bf16 instead
+    of turning into inf. A few V rows are scaled to ~1e5 in some key tiles:
+    O must stay finite and match the oracle (relative Frobenius 1e-2 per
+    (batch, head), the scale of O being ~1e5 there), LSE within 1e-3 (V does
+    not enter it), and tiles without such rows must keep the stated tolerance."""
+    import exact_attention_bf16_gb300 as ea
+    dqk, dv_ = dims
+    w = workloads.Workload("bigv", 1, 2, 700, 700, dqk, dv_, False, seed=31)
+    t = workloads.make_dense(w, device="cuda")
+    v = t["v"].clone()
+    v[0, 130] = 1.0e5   # in key tile 1
+    v[0, 600, 1] = -7.0e4  # in key tile 4, head 1 only
+    o, lse = ea.attn_fwd(t["q"], t["k"], v, softmax_scale=w.scale)
+    torch.cuda.synchronize()
+    ea.attn_get_device_status()
+    assert torch.isfinite(o.float()).all()
+    q, k, vv = (x.cpu() for x in (t["q"], t["k"], v))
+    for h in range(2):
+        o_ref, l_ref = attention_fwd(q[0, :, h], k[0, :, h], vv[0, :, h], w.scale, False)
+        got = o[0, :, h].cpu().double().numpy()
+        rel = np.linalg.norm(got - o_ref) / np.linalg.norm(o_ref)
+        assert rel <= 1e-2, (h, rel)
+        assert np.abs(lse[0, h].cpu().double().numpy() - l_ref).max() <= 1e-3
+    # the same problem with the large rows removed goes through fp16 throughout
+    o2, lse2 = ea.attn_fwd(t["q"], t["k"], t["v"], softmax_scale=w.scale)
+    torch.cuda.synchronize()
+    v0 = t["v"].cpu()
+    for h in range(2):
+        o_ref, l_ref = attention_fwd(q[0, :, h], k[0, :, h], v0[0, :, h], w.scale, False)
+        check_fwd(o2[0, :, h], lse2[0, h], o_ref, l_ref, f"bigv-free h{h}")
