@@ -561,24 +561,25 @@ def run_gpu(args):
 
 
 def run_case(args):
-    """A few launches of one pass on a small workload (B=2, H=16, N=8192, d=128;
-    268 MB of Q, K, V, O, larger than L2) for profiler captures."""
+    """A few launches of one pass on a small workload (B=2, H=16, N=8192, d_qk =
+    --dqk, d_v = min(d_qk, 128); Q, K, V, O of 67 to 100 MB each, larger than L2
+    together) for profiler captures."""
     import torch
     import __graft_entry__
     __graft_entry__.build()
     import exact_attention_bf16_gb300 as ea
     import workloads
-    w = workloads.Workload("case", 2, 16, 8192, 8192, 128, 128, args.causal, seed=0)
+    w = workloads.Workload("case", 2, 16, 8192, 8192, args.dqk, min(args.dqk, 128), args.causal, seed=0)
     t = workloads.make_dense(w, device="cuda")
     o, lse = ea.attn_fwd(t["q"], t["k"], t["v"], causal=w.causal)
     for _ in range(4):
         if args.case == "fwd":
-            ea.attn_fwd(t["q"], t["k"], t["v"], causal=w.causal, out=o, lse=lse)
+            ea.attn_fwd(t["q"], t["k"], t["v"], causal=w.causal, out=o, lse=lse, exp2_emu_period=args.emu)
         else:
-            ea.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=w.causal)
+            ea.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=w.causal, cta_pair=args.cta_pair)
     torch.cuda.synchronize()
     ea.attn_get_device_status()
-    print(f"case {args.case} causal={int(args.causal)} done")
+    print(f"case {args.case} d_qk={args.dqk} causal={int(args.causal)} emu={args.emu} pair={int(args.cta_pair)} done")
     return 0
 
 
@@ -586,6 +587,9 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", choices=["fwd", "bwd"], help="run a small profiling case and exit")
     ap.add_argument("--causal", action="store_true", help="causal mask for --case")
+    ap.add_argument("--dqk", type=int, default=128, choices=[64, 128, 192], help="head dim of Q/K for --case")
+    ap.add_argument("--emu", type=int, default=0, choices=[0, 4, 8], help="exp2 emulation period for --case fwd")
+    ap.add_argument("--cta-pair", action="store_true", help="two-SM dK/dV kernel for --case bwd")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)

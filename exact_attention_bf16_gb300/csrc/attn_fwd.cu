@@ -501,34 +501,39 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 }
 
 // V -> fp16 copy for the PV product (contiguous [rows, heads, d_v], rows = B * N
-// dense or total varlen). One 16-byte unit of 8 values per thread and step.
-// Sets *flag when a finite value lies outside fp16's range (|v| >= 65536,
-// which would become inf); inf and NaN convert to themselves.
+// dense or total varlen). One warp per token row: its heads x d_v values are
+// HEADS x DV / 8 units of 16 bytes, a warp-wide unit index split by constant
+// shifts, the (batch, row) division done once per row. Sets *flag when a
+// finite value lies outside fp16's range (|v| >= 65536, which would become
+// inf); inf and NaN convert to themselves.
+template <int DV>
 __global__ void v_to_f16_kernel(const void* v, int64_t sb, int64_t sn, int64_t sh, int nb, int nrows, int heads,
-                                int dv, void* out, uint32_t* flag) {
-  const int upr = dv / 8;  // 16-byte units per (row, head)
-  const int64_t units = static_cast<int64_t>(nb) * nrows * heads * upr;
+                                void* out, uint32_t* flag) {
+  constexpr int UPH = DV / 8;  // 16-byte units per (row, head)
+  const int upr = heads * UPH;  // per row
+  const int64_t rows = static_cast<int64_t>(nb) * nrows;
+  const int lane = static_cast<int>(threadIdx.x & 31u);
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   uint32_t bad = 0;
-  for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
-       u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int part = static_cast<int>(u % upr);
-    const int64_t rh = u / upr;  // (b, row, head), head fastest
-    const int h = static_cast<int>(rh % heads);
-    const int64_t br = rh / heads;
-    const int r = static_cast<int>(br % nrows), b = static_cast<int>(br / nrows);
-    const uint4 x = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(v) + b * sb + r * sn + h * sh +
-                                                    8 * part);
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    uint32_t o[4];
+  for (int64_t r = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; r < rows; r += nwarps) {
+    const int b = static_cast<int>(r / nrows), n = static_cast<int>(r % nrows);
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(v) + b * sb + n * sn;
+    uint4* dst = static_cast<uint4*>(out) + r * upr;
+#pragma unroll 4
+    for (int i = lane; i < upr; i += 32) {
+      const uint4 x = *reinterpret_cast<const uint4*>(src + (i / UPH) * sh + 8 * (i % UPH));
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      uint32_t o[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t lo = w[e] & 0x7FFFu, hi = (w[e] >> 16) & 0x7FFFu;
-      bad |= static_cast<uint32_t>(lo >= 0x4780u && lo < 0x7F80u) | static_cast<uint32_t>(hi >= 0x4780u && hi < 0x7F80u);
-      o[e] = pack_f16x2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t lo = w[e] & 0x7FFFu, hi = (w[e] >> 16) & 0x7FFFu;
+        bad |= static_cast<uint32_t>(lo >= 0x4780u && lo < 0x7F80u) | static_cast<uint32_t>(hi >= 0x4780u && hi < 0x7F80u);
+        o[e] = pack_f16x2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+      }
+      dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    reinterpret_cast<uint4*>(out)[u] = make_uint4(o[0], o[1], o[2], o[3]);
   }
-  if (__any_sync(0xffffffffu, bad != 0) && (threadIdx.x & 31u) == 0) atomicOr(flag, 1u);
+  if (__any_sync(0xffffffffu, bad != 0) && lane == 0) atomicOr(flag, 1u);
 }
 
 }  // namespace fwd
@@ -560,11 +565,13 @@ cudaError_t launch_fwd_diag_timeout(const CUtensorMap& tq, const CUtensorMap& tk
 
 cudaError_t launch_v_to_f16(const void* v, int64_t sb, int64_t sn, int64_t sh, int nb, int nrows, int heads, int dv,
                             void* out, uint32_t* flag, cudaStream_t stream) {
-  const int64_t units = static_cast<int64_t>(nb) * nrows * heads * (dv / 8);
-  if (units == 0) return cudaSuccess;
-  const int64_t blocks = (units + 255) / 256 < 152 * 16 ? (units + 255) / 256 : 152 * 16;
-  fwd::v_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(v, sb, sn, sh, nb, nrows, heads, dv, out,
-                                                                         flag);
+  const int64_t rows = static_cast<int64_t>(nb) * nrows;
+  if (rows == 0) return cudaSuccess;
+  const int64_t want = (rows + 7) / 8;  // 8 warps (rows) per block and pass
+  const unsigned blocks = static_cast<unsigned>(want < 152 * 8 ? want : 152 * 8);
+  if (dv == 64) fwd::v_to_f16_kernel<64><<<blocks, 256, 0, stream>>>(v, sb, sn, sh, nb, nrows, heads, out, flag);
+  else if (dv == 128) fwd::v_to_f16_kernel<128><<<blocks, 256, 0, stream>>>(v, sb, sn, sh, nb, nrows, heads, out, flag);
+  else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
