@@ -250,9 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool haveV = j > 0;
         const int uK = 2 * j, uV = 2 * (j - 1) + 1;
         const int sK = uK % C::NSLOT, sV = (uV + C::NSLOT) % C::NSLOT;
-        if (haveK) ok = mbar_wait(&bar->kv_full[sK], static_cast<uint32_t>(uK / C::NSLOT) & 1u, a.status, 0x210, lim);
+        const uint32_t js = (static_cast<uint32_t>(j) & 0xFFFu) << 12;  // the step, in the site's bits 12..23
+        if (haveK) ok = mbar_wait(&bar->kv_full[sK], static_cast<uint32_t>(uK / C::NSLOT) & 1u, a.status, 0x210 | js, lim);
         if (ok && haveV)
-          ok = mbar_wait(&bar->kv_full[sV], static_cast<uint32_t>(uV / C::NSLOT) & 1u, a.status, 0x211, lim);
+          ok = mbar_wait(&bar->kv_full[sV], static_cast<uint32_t>(uV / C::NSLOT) & 1u, a.status, 0x211 | js, lim);
         if (!ok) break;
         tc_fence_after();
         // descriptors built once per tile, advanced per k-step with one add
@@ -262,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < QT; ++i) {
           if (haveV && j - 1 < nkv[i]) {
             // O_i (+)= P_i(j-1) V_{j-1}: P from TMEM (aliasing S_i), V MN-major in shared memory
-            ok = mbar_wait(&bar->p_full[i], static_cast<uint32_t>(j - 1) & 1u, a.status, 0x220 + i, lim);
+            ok = mbar_wait(&bar->p_full[i], static_cast<uint32_t>(j - 1) & 1u, a.status, (0x220u + i) | js, lim);
             if (!ok) break;
             tc_fence_after();
             const uint32_t acc0 = j - 1 > 0 ? 1u : 0u;
@@ -310,7 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < nkv[i]; ++j) {
       const int kb = key_block(j);  // read before the wait, off the critical path
-      ok = mbar_wait_warp(&bar->s_full[i], static_cast<uint32_t>(j) & 1u, a.status, 0x300 + i, lim);
+      // site: 0x300 + tile, the step in bits 12..23 (a timeout then says where it stopped)
+      ok = mbar_wait_warp(&bar->s_full[i], static_cast<uint32_t>(j) & 1u, a.status,
+                          0x300u + i + ((static_cast<uint32_t>(j) & 0xFFFu) << 12), lim);
       if (!ok) break;
       tc_fence_after();
       uint32_t s[BN];

@@ -21,9 +21,19 @@ enum : uint32_t {
   DEV_BAD_CONFIG = 3,     // kernel saw a configuration it does not handle
 };
 
-// ~2^26 polls with nanosleep back-off ≈ several seconds at most: far above any
-// legitimate wait in these kernels, far below a watchdog.
-constexpr uint32_t kSpinLimit = 1u << 26;
+// A wait gives up after kWaitNs of wall time (read from %globaltimer): far
+// above any legitimate wait in these kernels, even when a profiler's
+// instrumented replay slows the waited-for role, and far below a watchdog.
+// A caller may pass a smaller poll-count limit instead (diagnostic launches);
+// kSpinLimit, the default, means "no poll limit, only the time limit".
+constexpr uint32_t kSpinLimit = 0xFFFFFFFFu;
+constexpr uint64_t kWaitNs = 10ull * 1000 * 1000 * 1000;
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ void record_error(uint32_t* status, uint32_t code, uint32_t where) {
   if (status) atomicCAS(status, 0u, (code << 24) | (where & 0xFFFFFFu));
@@ -71,18 +81,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits until the phase with the given parity has completed. Returns false
 // (and records DEV_TIMEOUT_MBAR) if it does not within `limit` polls.
+// Waits until the phase with the given parity has completed. Returns false
+// (and records DEV_TIMEOUT_MBAR at `where`) after kWaitNs, or after `limit`
+// polls when a smaller limit is given.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status, uint32_t where,
                                           uint32_t limit = kSpinLimit) {
   if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;  // try_wait itself suspends for a while
     // Back off only after ~1M polls: sleeping earlier delays the hand-offs on
     // the critical path (a woken MMA thread is hundreds of cycles late).
     if (i > (1u << 20)) __nanosleep(256);
-    // Another role or CTA already failed: stop waiting early (legitimate
-    // waits here last microseconds, never 2^16 polls).
-    if ((i & 0xFFFu) == 0xFFFu && i > (1u << 16) && status && *reinterpret_cast<volatile uint32_t*>(status) != 0)
-      return false;
+    if ((i & 0xFFFu) == 0xFFFu) {
+      // Another role or CTA already failed: stop waiting early (legitimate
+      // waits here last microseconds, never 2^16 polls).
+      if (i > (1u << 16) && status && *reinterpret_cast<volatile uint32_t*>(status) != 0) return false;
+      if (globaltimer_ns() - t0 > kWaitNs) break;
+    }
   }
   record_error(status, DEV_TIMEOUT_MBAR, where);
   return false;
@@ -322,11 +338,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 // the pair (acquire at cluster scope); bounded like mbar_wait.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t* status, uint32_t where) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if (i > (1u << 20)) __nanosleep(256);
-    if ((i & 0xFFFu) == 0xFFFu && i > (1u << 16) && status && *reinterpret_cast<volatile uint32_t*>(status) != 0)
-      return false;
+    if ((i & 0xFFFu) == 0xFFFu) {
+      if (i > (1u << 16) && status && *reinterpret_cast<volatile uint32_t*>(status) != 0) return false;
+      if (globaltimer_ns() - t0 > kWaitNs) break;
+    }
   }
   record_error(status, DEV_TIMEOUT_MBAR, where);
   return false;
