@@ -21,13 +21,16 @@ enum : uint32_t {
   DEV_BAD_CONFIG = 3,     // kernel saw a configuration it does not handle
 };
 
-// A wait gives up after kWaitNs of wall time (read from %globaltimer): far
-// above any legitimate wait in these kernels, even when a profiler's
-// instrumented replay slows the waited-for role, and far below a watchdog.
-// A caller may pass a smaller poll-count limit instead (diagnostic launches);
-// kSpinLimit, the default, means "no poll limit, only the time limit".
+// A wait gives up once it has lasted kWaitNs of wall time (%globaltimer) AND
+// polled at least kMinPolls times: far above any legitimate wait in these
+// kernels, far below a watchdog. Both are required because wall time alone
+// also advances while the kernel is paused (a profiler's replay, a debugger,
+// time-slicing), when no poll happens. A caller may pass a smaller poll-count
+// limit instead (diagnostic launches); kSpinLimit, the default, means "no
+// poll-count limit".
 constexpr uint32_t kSpinLimit = 0xFFFFFFFFu;
 constexpr uint64_t kWaitNs = 10ull * 1000 * 1000 * 1000;
+constexpr uint32_t kMinPolls = 1u << 22;
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
@@ -97,7 +100,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
       // Another role or CTA already failed: stop waiting early (legitimate
       // waits here last microseconds, never 2^16 polls).
       if (i > (1u << 16) && status && *reinterpret_cast<volatile uint32_t*>(status) != 0) return false;
-      if (globaltimer_ns() - t0 > kWaitNs) break;
+      if (i > kMinPolls && globaltimer_ns() - t0 > kWaitNs) break;
     }
   }
   record_error(status, DEV_TIMEOUT_MBAR, where);
@@ -344,7 +347,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     if (i > (1u << 20)) __nanosleep(256);
     if ((i & 0xFFFu) == 0xFFFu) {
       if (i > (1u << 16) && status && *reinterpret_cast<volatile uint32_t*>(status) != 0) return false;
-      if (globaltimer_ns() - t0 > kWaitNs) break;
+      if (i > kMinPolls && globaltimer_ns() - t0 > kWaitNs) break;
     }
   }
   record_error(status, DEV_TIMEOUT_MBAR, where);
