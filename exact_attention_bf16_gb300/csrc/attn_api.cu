@@ -223,17 +223,48 @@ struct SparseSpec {
   int32_t max_kv = 0;
 };
 
+// Tile list of a packed variable-length launch (launch_tile_list): one
+// 32-byte entry per CTA of a grid bounded by heads * (total / R + sequences),
+// plus 8 bytes of scratch per sequence. Not built (the grid covers the longest
+// sequence for every sequence instead) when a sequence may exceed
+// kMaxListBlocks blocks.
+struct ListPlan {
+  bool use = false;
+  int rows_per_block = 0, max_nblk = 0;
+  int64_t bound = 0;
+  size_t list_bytes = 0;
+};
+size_t round256(int64_t b) { return static_cast<size_t>((b + 255) / 256 * 256); }
+ListPlan list_plan(int64_t total_rows, int num_seqs, int heads, int64_t max_len, int rows_per_block) {
+  ListPlan lp;
+  const int64_t max_nblk = (max_len + rows_per_block - 1) / rows_per_block;
+  if (total_rows <= 0 || num_seqs < 1 || heads < 1 || max_nblk > kMaxListBlocks || max_nblk < 0) return lp;
+  lp.use = true;
+  lp.rows_per_block = rows_per_block;
+  lp.max_nblk = static_cast<int>(max_nblk);
+  lp.bound = static_cast<int64_t>(heads) * (total_rows / rows_per_block + num_seqs);
+  lp.list_bytes = round256(lp.bound * static_cast<int64_t>(sizeof(TileEntry)));
+  return lp;
+}
+size_t seq_scratch_bytes(int num_seqs) { return round256(static_cast<int64_t>(num_seqs) * 8); }
+
 // Forward workspace: a 256-byte block holding the range flag, then the fp16
-// copy of V ([rows, heads, d_v], contiguous) that the PV product reads.
+// copy of V ([rows, heads, d_v], contiguous) that the PV product reads, then
+// (packed variable length) the tile list and its scratch.
 size_t fwd_v16_bytes(const attn_fwd_params* p, bool varlen) {
   if (p->heads < 1 || p->d_v <= 0) return 0;
   const int64_t rows = varlen ? static_cast<int64_t>(p->total_k) : static_cast<int64_t>(p->batch) * p->seqlen_k;
   if (rows <= 0) return 0;
   return static_cast<size_t>((rows * p->heads * p->d_v * 2 + 255) / 256 * 256);
 }
+ListPlan fwd_list_plan(const attn_fwd_params* p, bool varlen) {
+  return varlen ? list_plan(p->total_q, p->num_seqs, p->heads, p->max_seqlen_q, 256) : ListPlan{};
+}
 size_t fwd_workspace_bytes(const attn_fwd_params* p, bool varlen) {
   const size_t v16 = fwd_v16_bytes(p, varlen);
-  return v16 ? 256 + v16 : 0;
+  if (!v16) return 0;
+  const ListPlan lp = fwd_list_plan(p, varlen);
+  return 256 + v16 + (lp.use ? lp.list_bytes + seq_scratch_bytes(p->num_seqs) : 0);
 }
 
 // diag_limit != 0: the diagnostic launch of attn_diag_wait_timeout instead of the forward.
@@ -319,6 +350,17 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
                         p->heads, p->d_v, v16, flag, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fwd V conversion");
   a.v16_flag = flag;
+  const ListPlan lp = fwd_list_plan(p, varlen);
+  if (lp.use) {  // longest sequences first, no CTA past a sequence's end
+    uint8_t* lbase = static_cast<uint8_t*>(ws) + 256 + fwd_v16_bytes(p, varlen);
+    TileEntry* list = reinterpret_cast<TileEntry*>(lbase);
+    int64_t* scratch = reinterpret_cast<int64_t*>(lbase + lp.list_bytes);
+    e = launch_tile_list(p->cu_seqlens_q, p->cu_seqlens_k, p->num_seqs, p->heads, 256, false, true, lp.max_nblk, list,
+                         scratch, lp.bound, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fwd tile list");
+    a.tiles = list;
+    a.n_tiles = lp.bound;
+  }
   e = sp.kv_count ? launch_fwd_sparse(p->d_qk, p->d_v, tq, tk, tv, tv16, a, stream)
                   : launch_fwd(p->d_qk, p->d_v, tq, tk, tv, tv16, a, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "fwd launch");
@@ -327,13 +369,30 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
 
 int bwd_dkdv_rows(int d_qk) { return d_qk == 128 ? 128 : 64; }  // query rows per step of the dK/dV kernel
 
-// Invalid (negative) shapes need no workspace: the call itself reports them.
-size_t bwd_workspace_bytes(const attn_bwd_params* p, bool varlen) {
+// Backward workspace: D (4 bytes per query row and head), then (packed
+// variable length) the dK/dV and dQ tile lists and their scratch. Invalid
+// (negative) shapes need no workspace: the call itself reports them.
+size_t bwd_d_bytes(const attn_bwd_params* p, bool varlen) {
   const attn_fwd_params& f = p->fwd;
   if (f.heads < 0 || (varlen ? f.total_q < 0 : (f.batch < 0 || f.seqlen_q < 0))) return 0;
   const int64_t rows = varlen ? static_cast<int64_t>(f.heads) * f.total_q
                               : static_cast<int64_t>(f.batch) * f.heads * f.seqlen_q;
-  return static_cast<size_t>((rows * 4 + 255) / 256 * 256);
+  return round256(rows * 4);
+}
+ListPlan bwd_kv_plan(const attn_bwd_params* p, bool varlen) {
+  const attn_fwd_params& f = p->fwd;
+  return varlen && !p->cta_pair ? list_plan(f.total_k, f.num_seqs, f.heads, f.max_seqlen_k, 128) : ListPlan{};
+}
+ListPlan bwd_q_plan(const attn_bwd_params* p, bool varlen) {
+  const attn_fwd_params& f = p->fwd;
+  return varlen ? list_plan(f.total_q, f.num_seqs, f.heads, f.max_seqlen_q, 128) : ListPlan{};
+}
+size_t bwd_workspace_bytes(const attn_bwd_params* p, bool varlen) {
+  const size_t d = bwd_d_bytes(p, varlen);
+  if (!varlen) return d;
+  const ListPlan kv = bwd_kv_plan(p, varlen), q = bwd_q_plan(p, varlen);
+  const size_t lists = (kv.use ? kv.list_bytes : 0) + (q.use ? q.list_bytes : 0);
+  return d + lists + (lists ? seq_scratch_bytes(p->fwd.num_seqs) : 0);
 }
 
 // Extra workspace of the block-sparse backward: the transposed lists
@@ -410,6 +469,29 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
   }
   cudaError_t e = status_ptr(&a.status);
   if (e != cudaSuccess) return cuda_fail(e, "status word");
+
+  if (nq_rows > 0 && nk_rows > 0 && varlen) {  // tile lists: longest sequences first, no CTA past an end
+    const ListPlan kv = bwd_kv_plan(p, varlen), qp = bwd_q_plan(p, varlen);
+    uint8_t* lbase = static_cast<uint8_t*>(ws) + bwd_d_bytes(p, varlen);
+    int64_t* scratch = reinterpret_cast<int64_t*>(lbase + (kv.use ? kv.list_bytes : 0) + (qp.use ? qp.list_bytes : 0));
+    if (kv.use) {
+      TileEntry* list = reinterpret_cast<TileEntry*>(lbase);
+      e = launch_tile_list(f.cu_seqlens_q, f.cu_seqlens_k, f.num_seqs, f.heads, 128, true, false, kv.max_nblk, list,
+                           scratch, kv.bound, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "bwd tile list");
+      a.tiles_kv = list;
+      a.n_tiles_kv = kv.bound;
+      lbase += kv.list_bytes;
+    }
+    if (qp.use) {
+      TileEntry* list = reinterpret_cast<TileEntry*>(lbase);
+      e = launch_tile_list(f.cu_seqlens_q, f.cu_seqlens_k, f.num_seqs, f.heads, 128, false, true, qp.max_nblk, list,
+                           scratch, qp.bound, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "bwd tile list");
+      a.tiles_q = list;
+      a.n_tiles_q = qp.bound;
+    }
+  }
 
   if (nq_rows == 0 || nk_rows == 0) {
     // Nothing to differentiate through: no queries -> dK = dV = 0; no keys -> dQ = 0.

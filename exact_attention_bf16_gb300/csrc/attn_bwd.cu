@@ -169,10 +169,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (unit, head) is the slow index so that resident CTAs share a few heads'
   // Q/dO in L2; within a head the heaviest key tiles (tile 0 sees every query
   // under the causal mask) come first.
-  const int bh = static_cast<int>(blockIdx.x) / a.n_kblk;
-  const int n = static_cast<int>(blockIdx.x) % a.n_kblk;
-  const int h = bh % a.heads;
-  const Unit U = unit_bounds(a, bh / a.heads);
+  Unit U;
+  int h, n;
+  if (!bwd_work(a, a.tiles_kv, a.n_kblk, false, U, h, n)) return;
   const int k0 = n * KB;
   if (k0 >= U.nk) return;
   int m_begin = 0;
@@ -548,10 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   DkdvWBars* bar = reinterpret_cast<DkdvWBars*>(smem_w + C::OFF_BAR);
 
   // same work order as dkdv_kernel: (unit, head) slow, key tile 0 (the heaviest under causal) first
-  const int bh = static_cast<int>(blockIdx.x) / a.n_kblk;
-  const int n = static_cast<int>(blockIdx.x) % a.n_kblk;
-  const int h = bh % a.heads;
-  const Unit U = unit_bounds(a, bh / a.heads);
+  Unit U;
+  int h, n;
+  if (!bwd_work(a, a.tiles_kv, a.n_kblk, false, U, h, n)) return;
   const int k0 = n * KB;
   if (k0 >= U.nk) return;
   int m_begin = 0;
@@ -962,10 +960,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   DqBars* bar = reinterpret_cast<DqBars*>(smem + C::OFF_BAR);
 
   // (unit, head) slow for L2 sharing of K/V; heaviest (last) query tiles first within a head
-  const int bh = static_cast<int>(blockIdx.x) / a.n_qblk;
-  const int m = a.n_qblk - 1 - static_cast<int>(blockIdx.x) % a.n_qblk;
-  const int h = bh % a.heads;
-  const Unit U = unit_bounds(a, bh / a.heads);
+  Unit U;
+  int h, m;
+  if (!bwd_work(a, a.tiles_q, a.n_qblk, true, U, h, m)) return;
   const int q0 = m * MB;
   if (q0 >= U.nq) return;
   const int last = min(q0 + MB - 1, U.nq - 1);
@@ -1269,7 +1266,7 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   static PerDeviceOnce once;
   cudaError_t e = once.run([&] { return set_smem(kern, C::SMEM); });
   if (e != cudaSuccess) return e;
-  const int64_t grid = static_cast<int64_t>(a.n_kblk) * a.num_units * a.heads;
+  const int64_t grid = a.tiles_kv ? a.n_tiles_kv : static_cast<int64_t>(a.n_kblk) * a.num_units * a.heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, a);
@@ -1282,7 +1279,7 @@ cudaError_t launch_dkdv_wide(const CUtensorMap& tq, const CUtensorMap& tk, const
   static PerDeviceOnce once;
   cudaError_t e = once.run([] { return set_smem(dkdv_wide_kernel<SPARSE>, DkdvWCfg::SMEM); });
   if (e != cudaSuccess) return e;
-  const int64_t grid = static_cast<int64_t>(a.n_kblk) * a.num_units * a.heads;
+  const int64_t grid = a.tiles_kv ? a.n_tiles_kv : static_cast<int64_t>(a.n_kblk) * a.num_units * a.heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   dkdv_wide_kernel<SPARSE><<<static_cast<unsigned>(grid), kThreads, DkdvWCfg::SMEM, stream>>>(tq, tk, tv, tdo, a);
@@ -1297,7 +1294,7 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   static PerDeviceOnce once;
   cudaError_t e = once.run([&] { return set_smem(kern, C::SMEM); });
   if (e != cudaSuccess) return e;
-  const int64_t grid = static_cast<int64_t>(a.n_qblk) * a.num_units * a.heads;
+  const int64_t grid = a.tiles_q ? a.n_tiles_q : static_cast<int64_t>(a.n_qblk) * a.num_units * a.heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, a);

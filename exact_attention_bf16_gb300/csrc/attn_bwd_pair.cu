@@ -456,7 +456,8 @@ cudaError_t launch_bwd_dkdv_pair(const CUtensorMap& tq_r, const CUtensorMap& tq_
                                  const CUtensorMap& tv, const CUtensorMap& tdo_r, const CUtensorMap& tdo_c,
                                  const BwdArgs& a, cudaStream_t stream) {
   using namespace bwd;
-  if (a.kv_count != nullptr) return cudaErrorInvalidValue;  // block-sparse lists use the one-SM kernel
+  // block-sparse lists use the one-SM kernel; a packed batch's pairs are decoded from the grid
+  if (a.kv_count != nullptr || a.tiles_kv != nullptr) return cudaErrorInvalidValue;
   static PerDeviceOnce once;
   cudaError_t e = once.run([] {
     return cudaFuncSetAttribute(dkdv_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvPCfg::SMEM);

@@ -103,7 +103,12 @@ __device__ __forceinline__ int key_limit(int row, int nq, int nk, int causal) {
 // and every wait gives up after a.spin_limit polls, so the MMA and softmax
 // waits run out, record DEV_TIMEOUT_MBAR and the kernel returns with nothing
 // in flight (no copy or MMA was ever issued).
-template <int DQK, int DV, int EMU_PERIOD, bool SPARSE = false, bool DIAG = false>
+//
+// LIST (packed variable length): the CTA's (sequence, head, block) comes from
+// the tile list in a.tiles instead of the block index. A variant of its own, so
+// that the dense kernels keep their bounds in the constant bank rather than in
+// registers.
+template <int DQK, int DV, int EMU_PERIOD, bool SPARSE = false, bool DIAG = false, bool LIST = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmv16,
@@ -119,17 +124,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (unit, head) is the slow index so that the CTAs resident at any time share
   // a few heads' K/V in L2 (all heads' K/V together exceed it); within a head
   // the heaviest (last, under the causal mask) 256-row blocks come first.
-  const int bh = static_cast<int>(blockIdx.x) / a.n_mblk;
-  const int mblk = a.n_mblk - 1 - static_cast<int>(blockIdx.x) % a.n_mblk;
-  const int unit = bh / a.heads;
-  const int h = bh % a.heads;
-  int q_start = 0, k_start = 0, nq = a.seqlen_q, nk = a.seqlen_k, b = unit;
-  if (a.cu_q != nullptr) {
-    q_start = a.cu_q[unit];
-    nq = a.cu_q[unit + 1] - q_start;
-    k_start = a.cu_k[unit];
-    nk = a.cu_k[unit + 1] - k_start;
-    b = 0;
+  int mblk, h, q_start = 0, k_start = 0, nq = a.seqlen_q, nk = a.seqlen_k, b;
+  if constexpr (LIST) {
+    // packed variable length: this CTA's entry of the tile list (longest sequences first)
+    const int4* te = reinterpret_cast<const int4*>(a.tiles + blockIdx.x);
+    const int4 t0 = __ldg(te), t1 = __ldg(te + 1);
+    if (t1.z < 0) return;  // an empty entry past the real ones
+    q_start = t0.x, nq = t0.y, k_start = t0.z, nk = t0.w, h = t1.x, mblk = t1.y, b = 0;
+  } else {
+    const int bh = static_cast<int>(blockIdx.x) / a.n_mblk;
+    mblk = a.n_mblk - 1 - static_cast<int>(blockIdx.x) % a.n_mblk;
+    const int unit = bh / a.heads;
+    h = bh % a.heads;
+    b = unit;
+    if (a.cu_q != nullptr) {
+      q_start = a.cu_q[unit];
+      nq = a.cu_q[unit + 1] - q_start;
+      k_start = a.cu_k[unit];
+      nk = a.cu_k[unit + 1] - k_start;
+      b = 0;
+    }
   }
   const int row0 = mblk * (QT * BM);
   if (row0 >= nq) return;  // block-uniform: this unit is shorter than the grid's longest
@@ -166,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   const int nkv_max = max(nkv[0], nkv[1]);
-  const uint32_t lim = DIAG ? a.spin_limit : kSpinLimit;  // poll limit of the waits below
+  const PollLimit poll_lim = DIAG ? PollLimit{a.spin_limit} : kNoPollLimit;  // of the waits below
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -243,17 +257,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
       const uint32_t idO = v_is_f16(a) ? idesc_f16_f32(BM, DV, false, true) : idesc_bf16_f32(BM, DV, false, true);
-      bool ok = mbar_wait(&bar->q_full[0], 0, a.status, 0x200, lim) &&
-                mbar_wait(&bar->q_full[1], 0, a.status, 0x201, lim);
+      bool ok = mbar_wait(&bar->q_full[0], 0, a.status, 0x200, poll_lim) &&
+                mbar_wait(&bar->q_full[1], 0, a.status, 0x201, poll_lim);
       for (int j = 0; j <= nkv_max && ok; ++j) {
         const bool haveK = j < nkv_max;
         const bool haveV = j > 0;
         const int uK = 2 * j, uV = 2 * (j - 1) + 1;
         const int sK = uK % C::NSLOT, sV = (uV + C::NSLOT) % C::NSLOT;
         const uint32_t js = (static_cast<uint32_t>(j) & 0xFFFu) << 12;  // the step, in the site's bits 12..23
-        if (haveK) ok = mbar_wait(&bar->kv_full[sK], static_cast<uint32_t>(uK / C::NSLOT) & 1u, a.status, 0x210 | js, lim);
+        if (haveK) ok = mbar_wait(&bar->kv_full[sK], static_cast<uint32_t>(uK / C::NSLOT) & 1u, a.status, 0x210 | js, poll_lim);
         if (ok && haveV)
-          ok = mbar_wait(&bar->kv_full[sV], static_cast<uint32_t>(uV / C::NSLOT) & 1u, a.status, 0x211 | js, lim);
+          ok = mbar_wait(&bar->kv_full[sV], static_cast<uint32_t>(uV / C::NSLOT) & 1u, a.status, 0x211 | js, poll_lim);
         if (!ok) break;
         tc_fence_after();
         // descriptors built once per tile, advanced per k-step with one add
@@ -263,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < QT; ++i) {
           if (haveV && j - 1 < nkv[i]) {
             // O_i (+)= P_i(j-1) V_{j-1}: P from TMEM (aliasing S_i), V MN-major in shared memory
-            ok = mbar_wait(&bar->p_full[i], static_cast<uint32_t>(j - 1) & 1u, a.status, (0x220u + i) | js, lim);
+            ok = mbar_wait(&bar->p_full[i], static_cast<uint32_t>(j - 1) & 1u, a.status, (0x220u + i) | js, poll_lim);
             if (!ok) break;
             tc_fence_after();
             const uint32_t acc0 = j - 1 > 0 ? 1u : 0u;
@@ -301,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t quarter = warp & 3u;    // TMEM lane quarter this warp may access
     const int row_in_tile = static_cast<int>(quarter * 32 + lane);
     const int row = row0 + i * BM + row_in_tile;
-    const int lim = key_limit(row, nq, nk, a.causal);
+    const int klim = key_limit(row, nq, nk, a.causal);  // keys visible to this row
     const uint32_t lane_base = tbase + ((quarter * 32u) << 16);
     const float sl2 = a.scale_log2;
     const bool f16 = v_is_f16(a);  // P packed as fp16 (V's copy) or bf16
@@ -313,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kb = key_block(j);  // read before the wait, off the critical path
       // site: 0x300 + tile, the step in bits 12..23 (a timeout then says where it stopped)
       ok = mbar_wait_warp(&bar->s_full[i], static_cast<uint32_t>(j) & 1u, a.status,
-                          0x300u + i + ((static_cast<uint32_t>(j) & 0xFFFu) << 12), lim);
+                          0x300u + i + ((static_cast<uint32_t>(j) & 0xFFFu) << 12), poll_lim);
       if (!ok) break;
       tc_fence_after();
       uint32_t s[BN];
@@ -322,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(lane_base + tS(i) + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
       tmem_ld32(lane_base + tS(i) + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
       tmem_wait_ld();
-      const int cnt = lim - kb * BN;  // visible keys of this row inside the tile
+      const int cnt = klim - kb * BN;  // visible keys of this row inside the tile
       if (cnt < BN) {
 #pragma unroll
         for (int c = 0; c < BN; ++c)
@@ -404,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ---- epilogue: O = acc / l (exact normalisation), LSE = ln2 * (m + log2 l)
     if (ok && nkv[i] > 0) {
-      ok = mbar_wait_warp(&bar->o_full[i], 0, a.status, 0x310 + i, lim);
+      ok = mbar_wait_warp(&bar->o_full[i], 0, a.status, 0x310 + i, poll_lim);
       tc_fence_after();
     }
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
@@ -467,11 +481,11 @@ __global__ void exp2_eval_kernel(const float* x, float* yp, float* yh, int64_t n
   }
 }
 
-template <int DQK, int DV, int EMU, bool SPARSE = false, bool DIAG = false>
+template <int DQK, int DV, int EMU, bool SPARSE = false, bool DIAG = false, bool LIST = false>
 cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tv16,
                      const FwdArgs& a, cudaStream_t stream) {
   using C = Cfg<DQK, DV>;
-  auto kern = attn_fwd_kernel<DQK, DV, EMU, SPARSE, DIAG>;
+  auto kern = attn_fwd_kernel<DQK, DV, EMU, SPARSE, DIAG, LIST>;
   static PerDeviceOnce once;
   cudaError_t e = once.run([&]() -> cudaError_t {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -483,7 +497,8 @@ cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     return fa.numRegs * kThreads < C::REG_BUDGET ? cudaErrorInvalidConfiguration : cudaSuccess;
   });
   if (e != cudaSuccess) return e;
-  const int64_t grid = static_cast<int64_t>(a.n_mblk) * a.num_units * a.heads;
+  if (LIST != (a.tiles != nullptr)) return cudaErrorInvalidValue;
+  const int64_t grid = LIST ? a.n_tiles : static_cast<int64_t>(a.n_mblk) * a.num_units * a.heads;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM, stream>>>(tq, tk, tv, tv16, a);
@@ -495,6 +510,14 @@ cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 template <int DQK, int DV>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tv16,
                      const FwdArgs& a, cudaStream_t stream) {
+  if (a.tiles != nullptr) {
+    switch (a.emu_period) {
+      case 0: return launch_e<DQK, DV, 0, false, false, true>(tq, tk, tv, tv16, a, stream);
+      case 4: return launch_e<DQK, DV, 4, false, false, true>(tq, tk, tv, tv16, a, stream);
+      case 8: return launch_e<DQK, DV, 8, false, false, true>(tq, tk, tv, tv16, a, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (a.emu_period) {
     case 0: return launch_e<DQK, DV, 0>(tq, tk, tv, tv16, a, stream);
     case 4: return launch_e<DQK, DV, 4>(tq, tk, tv, tv16, a, stream);
@@ -551,7 +574,8 @@ cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorM
 
 cudaError_t launch_fwd_sparse(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tv16, const FwdArgs& a, cudaStream_t stream) {
-  if (a.cu_q != nullptr || a.emu_period != 0 || a.kv_count == nullptr || a.max_kv < 0) return cudaErrorInvalidValue;
+  if (a.cu_q != nullptr || a.tiles != nullptr || a.emu_period != 0 || a.kv_count == nullptr || a.max_kv < 0)
+    return cudaErrorInvalidValue;
   if (a.max_kv > 0 && a.kv_index == nullptr) return cudaErrorInvalidValue;
   if (d_qk == 64 && d_v == 64) return fwd::launch_e<64, 64, 0, true>(tq, tk, tv, tv16, a, stream);
   if (d_qk == 128 && d_v == 128) return fwd::launch_e<128, 128, 0, true>(tq, tk, tv, tv16, a, stream);
@@ -561,7 +585,7 @@ cudaError_t launch_fwd_sparse(int d_qk, int d_v, const CUtensorMap& tq, const CU
 
 cudaError_t launch_fwd_diag_timeout(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const FwdArgs& a, cudaStream_t stream) {
-  if (a.cu_q != nullptr || a.kv_count != nullptr || a.spin_limit == 0 || a.v16_flag != nullptr)
+  if (a.cu_q != nullptr || a.tiles != nullptr || a.kv_count != nullptr || a.spin_limit == 0 || a.v16_flag != nullptr)
     return cudaErrorInvalidValue;
   return fwd::launch_e<64, 64, 0, false, true>(tq, tk, tv, tv, a, stream);
 }

@@ -38,5 +38,29 @@ __device__ __forceinline__ Unit unit_bounds(const BwdArgs& a, int unit) {
   return u;
 }
 
+// A backward CTA's work: from the tile list of a packed variable-length
+// launch (`tiles` non-null), else from the block index over nblk blocks per
+// (unit, head), blocks in descending (dQ: the last query blocks are the
+// heaviest under the causal mask) or ascending (dK/dV: the first key blocks)
+// order. Returns false for an empty list entry (the CTA has no work).
+__device__ __forceinline__ bool bwd_work(const BwdArgs& a, const TileEntry* tiles, int nblk, bool descending,
+                                         Unit& U, int& h, int& blk) {
+  if (tiles != nullptr) {
+    const int4* te = reinterpret_cast<const int4*>(tiles + blockIdx.x);
+    const int4 t0 = __ldg(te), t1 = __ldg(te + 1);
+    if (t1.z < 0) return false;
+    U = Unit{0, t0.x, t0.z, t0.y, t0.w};
+    h = t1.x;
+    blk = t1.y;
+    return true;
+  }
+  const int bh = static_cast<int>(blockIdx.x) / nblk;
+  const int r = static_cast<int>(blockIdx.x) % nblk;
+  blk = descending ? nblk - 1 - r : r;
+  h = bh % a.heads;
+  U = unit_bounds(a, bh / a.heads);
+  return true;
+}
+
 }  // namespace bwd
 }  // namespace gb300

@@ -48,6 +48,26 @@ class DeviceScope {
   bool switched_ = false;
 };
 
+// One CTA's work in a packed variable-length launch (built by
+// launch_tile_list): the sequence's row ranges, the head and the block index
+// (of R rows: 256 queries forward, 128 keys dK/dV, 128 queries dQ). seq < 0:
+// an empty entry past the real ones; its CTA exits.
+struct TileEntry {
+  int q_start, nq, k_start, nk;
+  int head, blk, seq, pad;
+};
+static_assert(sizeof(TileEntry) == 32, "two 16-byte loads per CTA");
+constexpr int kMaxListBlocks = 2047;  // longest sequence, in blocks, a list is built for
+
+// Builds the list for num_seqs sequences (cu_q / cu_k offsets on the device):
+// sequences with the most blocks first (by key blocks when by_keys), then
+// head by head, blocks of a head in descending or ascending order. Writes
+// `bound` entries (the real ones, then empty ones); seq_start is scratch of
+// num_seqs int64. max_nblk bounds every sequence's block count (<= kMaxListBlocks).
+cudaError_t launch_tile_list(const int* cu_q, const int* cu_k, int num_seqs, int heads, int rows_per_block,
+                             bool by_keys, bool descending, int max_nblk, TileEntry* out, int64_t* seq_start,
+                             int64_t bound, cudaStream_t stream);
+
 // Forward kernel arguments (passed by value; tensor maps go separately as
 // __grid_constant__ parameters).
 struct FwdArgs {
@@ -75,6 +95,10 @@ struct FwdArgs {
   // fp16 copy (map tv16) and P is packed in fp16; nonzero, or a null pointer,
   // = V and P in bf16.
   const uint32_t* v16_flag;
+  // Packed variable-length only (nullptr otherwise): one entry per CTA, and
+  // the number of entries (the grid).
+  const TileEntry* tiles;
+  int64_t n_tiles;
 };
 
 cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -135,6 +159,12 @@ struct BwdArgs {
   const int* q_count;
   const int* q_index;
   int n_qb256;
+  // Packed variable-length only (nullptr otherwise): the dK/dV kernels' list
+  // (128-key blocks) and the dQ kernel's (128-query blocks), with their sizes.
+  const TileEntry* tiles_kv;
+  int64_t n_tiles_kv;
+  const TileEntry* tiles_q;
+  int64_t n_tiles_q;
 };
 
 // D = rowsum(dO * O) into args.dsum.

@@ -26,9 +26,13 @@ enum : uint32_t {
 // kernels, far below a watchdog. Both are required because wall time alone
 // also advances while the kernel is paused (a profiler's replay, a debugger,
 // time-slicing), when no poll happens. A caller may pass a smaller poll-count
-// limit instead (diagnostic launches); kSpinLimit, the default, means "no
-// poll-count limit".
-constexpr uint32_t kSpinLimit = 0xFFFFFFFFu;
+// limit instead (diagnostic launches); kNoPollLimit, the default, means "no
+// poll-count limit". The limit has a type of its own so that no other integer
+// (a row's key count, say) can be passed for it by mistake.
+struct PollLimit {
+  uint32_t n;
+};
+constexpr PollLimit kNoPollLimit{0xFFFFFFFFu};
 constexpr uint64_t kWaitNs = 10ull * 1000 * 1000 * 1000;
 constexpr uint32_t kMinPolls = 1u << 22;
 
@@ -88,10 +92,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // (and records DEV_TIMEOUT_MBAR at `where`) after kWaitNs, or after `limit`
 // polls when a smaller limit is given.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status, uint32_t where,
-                                          uint32_t limit = kSpinLimit) {
+                                          PollLimit limit = kNoPollLimit) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 0; i < limit; ++i) {
+  for (uint32_t i = 0; i < limit.n; ++i) {
     if (mbar_try_wait(bar, parity)) return true;  // try_wait itself suspends for a while
     // Back off only after ~1M polls: sleeping earlier delays the hand-offs on
     // the critical path (a woken MMA thread is hundreds of cycles late).
@@ -111,7 +115,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 // warp-collective instructions (tcgen05.ld/st, votes) afterwards: if any lane's
 // wait failed, every lane sees false, so the warp leaves its loop as one.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status, uint32_t where,
-                                               uint32_t limit = kSpinLimit) {
+                                               PollLimit limit = kNoPollLimit) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, where, limit));
 }
 

@@ -83,7 +83,14 @@ typedef void* attn_stream_t;
  * cu_seqlens_k are device int32 arrays of num_seqs+1 non-decreasing offsets
  * starting at 0; total_q / total_k are the packed row counts (= last offset),
  * max_seqlen_q / max_seqlen_k bound every sequence's length; batch and the
- * batch strides are ignored. */
+ * batch strides are ignored. Work scheduling (the tile scheduler for
+ * variable-length balance of newton wiki "FlashAttention-4", 核心技術): when
+ * max_seqlen_q <= 2047 x 256 (forward), or max_seqlen_q and max_seqlen_k <=
+ * 2047 x 128 (backward, per kernel), the call first builds on the stream, in
+ * its workspace, a list with one entry per real block of rows, the sequences
+ * with the most blocks first, and launches one CTA per entry; otherwise each
+ * sequence gets a grid slice sized for max_seqlen. The results are the same
+ * bits either way. */
 typedef struct attn_fwd_params {
   const void* q;
   const void* k;
@@ -166,7 +173,14 @@ typedef struct attn_bwd_params {
  * row. Its size is 256 + 2 * (keys x heads x d_v) bytes, rounded up to 256;
  * it must be 256-byte aligned. When V holds a finite value with |v| >= 65536
  * (outside fp16's range), that call computes the PV product in bf16
- * instead. */
+ * instead. A variable-length forward that builds its tile list adds, each
+ * rounded up to 256, 32 x heads x (total_q / 256 + num_seqs) bytes for the
+ * list and 8 x num_seqs bytes of scratch.
+ * The backward's workspace holds D = rowsum(dO * O): 4 x heads x query rows
+ * bytes, rounded up to 256, 16-byte aligned; a variable-length backward adds
+ * its tile lists, 32 x heads x (total_k / 128 + num_seqs) bytes for dK/dV
+ * (none with cta_pair) and 32 x heads x (total_q / 128 + num_seqs) for dQ, and
+ * 8 x num_seqs bytes of scratch, each rounded up to 256. */
 size_t attn_fwd_workspace_size(const attn_fwd_params* p);
 size_t attn_bwd_workspace_size(const attn_bwd_params* p);
 
@@ -220,7 +234,8 @@ attn_status_t attn_bwd_block_sparse(const attn_bwd_params* p, const int32_t* kv_
  * until process exit. The attention method has no counterpart to this entry
  * point; it exists only for these callers. Limit: attn_bwd_workspace_size(p)
  * must not exceed ATTN_BWD_NOALLOC_SCRATCH_BYTES (4 bytes per batch x head x
- * query row, so up to 2,097,152 such rows), else ATTN_ERR_WORKSPACE and
+ * query row, so up to 2,097,152 such rows dense; variable length adds the
+ * tile lists), else ATTN_ERR_WORKSPACE and
  * nothing is launched. The first call on each device resolves the array's
  * address and should come before any stream capture. All calls share the one
  * array: calls that may overlap on the GPU race and must be serialised by the

@@ -250,4 +250,31 @@ def test_fwd_workspace_size_holds_the_fp16_copy_of_v(lib, _abi):
     p = _valid_fwd(_abi)
     p.cu_seqlens_q = p.cu_seqlens_k = 0x10000
     p.num_seqs, p.total_q, p.total_k, p.max_seqlen_q, p.max_seqlen_k = 2, 300, 301, 200, 200
-    assert lib.attn_fwd_workspace_size(ctypes.byref(p)) == 256 + (301 * 4 * 64 * 2 + 255) // 256 * 256
+    # packed variable length adds the tile list: heads * (total_q // 256 + sequences)
+    # entries of 32 bytes, then 8 bytes per sequence of scratch, each rounded to 256
+    r256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    v16 = r256(301 * 4 * 64 * 2)
+    assert lib.attn_fwd_workspace_size(ctypes.byref(p)) == 256 + v16 + r256(32 * 4 * (300 // 256 + 2)) + r256(8 * 2)
+    p.max_seqlen_q = 2047 * 256 + 1  # a sequence may exceed the list's block limit: no list
+    p.total_q = p.total_k = 2047 * 256 + 1
+    assert lib.attn_fwd_workspace_size(ctypes.byref(p)) == 256 + r256(p.total_k * 4 * 64 * 2)
+
+
+def test_bwd_workspace_size_holds_the_tile_lists(lib, _abi):
+    """Packed variable length: D (4 bytes per query row and head), the dK/dV list
+    (128 keys per block), the dQ list (128 queries per block), the scratch."""
+    r256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    p = _abi.AttnBwdParams()
+    p.fwd = _valid_fwd(_abi)
+    f = p.fwd
+    f.cu_seqlens_q = f.cu_seqlens_k = 0x10000
+    f.num_seqs, f.total_q, f.total_k, f.max_seqlen_q, f.max_seqlen_k = 2, 300, 301, 200, 200
+    d = r256(4 * 4 * 300)
+    kv = r256(32 * 4 * (301 // 128 + 2))
+    q = r256(32 * 4 * (300 // 128 + 2))
+    assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == d + kv + q + r256(8 * 2)
+    p.cta_pair = 1  # the two-SM dK/dV kernel takes no list
+    assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == d + q + r256(8 * 2)
+    p.cta_pair = 0
+    f.cu_seqlens_q = f.cu_seqlens_k = 0  # dense: D only
+    assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == r256(4 * 4 * 128)
