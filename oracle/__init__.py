@@ -12,7 +12,8 @@ Contents
 attention.py  the plain definition of attention (dense softmax-then-matmul),
               forward and backward, dense and variable-length; and the
               conditional-rescale online-softmax algorithm restated in fp64;
-              the key visibility of a block-sparse mask, element by element.
+              the key visibility of a block-sparse mask, element by element;
+              the score modifications (logit soft-capping, ALiBi distance bias).
 exp2_poly.py  the Cody-Waite split + degree-3 polynomial exp2 emulation, with
               its own minimax (Remez exchange) coefficient fit.
 
@@ -27,6 +28,8 @@ from .attention import (  # noqa: F401
     attention_fwd_varlen,
     attention_bwd_varlen,
     block_sparse_visible,
+    head_score_mod,
+    score_mod_apply,
     visible_limit,
 )
 from .exp2_poly import fit_exp2_poly_remez, exp2_poly, exp2_exact  # noqa: F401

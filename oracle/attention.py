@@ -18,6 +18,11 @@ Sources
 * Backward (dQ, dK, dV for the loss <O, dO>), including the dQ reduction over
   the key dimension: wittx "FlashAttention-4", section 反向传播的优化. The pages
   give no formulas; the gradients below are the calculus of the definition.
+* Score modifications (FlexAttention variants built on FA4: wittx
+  "FlashAttention-4", section Python写GPU内核; newton wiki "FlashAttention-4",
+  發展歷程). The pages name FlexAttention but no modification; the two below
+  are its standard examples, applied to the scaled logit a_ij before the mask
+  and the softmax (see :func:`score_mod_apply`).
 
 Conventions (readings where the pages are silent)
 -------------------------------------------------
@@ -53,16 +58,44 @@ def visible_limit(i, nq: int, nk: int, causal: bool):
     return np.clip(i + (nk - nq) + 1, 0, nk).astype(np.int64)
 
 
-def _logits(q, k, softmax_scale, rows, nq, nk, causal, visible=None):
-    """a_ij = scale * q_i . k_j for visible j, -inf elsewhere (rows = row indices).
-    ``visible`` (optional bool [Nq, Nk]) hides further keys (AND with the causal mask)."""
-    a = softmax_scale * (q[rows] @ k.T)
+def _logits(q, k, softmax_scale, rows, nq, nk, causal, visible=None, score_mod=None, with_deriv=False):
+    """a_ij = mod(scale * q_i . k_j) for visible j, -inf elsewhere (rows = row indices).
+    ``visible`` (optional bool [Nq, Nk]) hides further keys (AND with the causal mask);
+    ``score_mod`` as in :func:`score_mod_apply`. With ``with_deriv`` also returns
+    the modification's derivative."""
+    a, da = score_mod_apply(softmax_scale * (q[rows] @ k.T), rows, nq, nk, score_mod)
     lim = visible_limit(rows, nq, nk, causal)
     cols = np.arange(nk)
     a[cols[None, :] >= lim[:, None]] = -np.inf
     if visible is not None:
         a[~np.asarray(visible, dtype=bool)[rows]] = -np.inf
-    return a
+    return (a, da) if with_deriv else a
+
+
+def score_mod_apply(a, rows, nq: int, nk: int, score_mod):
+    """A score modification of the scaled logits a = scale * q_i . k_j (rows:
+    the query indices of a's rows; all nk keys as columns).
+
+    * ``None``: a unchanged.
+    * ``("softcap", c)``, c > 0: a' = c * tanh(a / c) (logits soft-capped to (-c, c)).
+    * ``("alibi", m)``, m >= 0: a' = a - m * |j - (i + nk - nq)|, a linear penalty on the
+      distance between key j and query i, with the query's position aligned
+      bottom-right like the causal mask.
+
+    Returns (a', da'/da), the derivative elementwise (1 for the additive bias).
+    """
+    if score_mod is None:
+        return a, np.ones_like(a)
+    kind, val = score_mod
+    if kind == "softcap":
+        c = float(val)
+        t = np.tanh(a / c)
+        return c * t, 1.0 - t * t
+    if kind == "alibi":
+        qpos = np.asarray(rows)[:, None] + (nk - nq)
+        dist = np.abs(np.arange(nk)[None, :] - qpos)
+        return a - float(val) * dist, np.ones_like(a)
+    raise ValueError(f"unknown score modification {kind!r}")
 
 
 def block_sparse_visible(nq: int, nk: int, kv_count, kv_index, q_block: int = 256, k_block: int = 128):
@@ -94,7 +127,8 @@ def _row_blocks(nq: int, row_block):
         yield np.arange(r0, min(nq, r0 + rb))
 
 
-def attention_fwd(q, k, v, softmax_scale: float, causal: bool = False, row_block=None, visible=None):
+def attention_fwd(q, k, v, softmax_scale: float, causal: bool = False, row_block=None, visible=None,
+                  score_mod=None):
     """Dense definition of one head's forward pass.
 
     O_i = sum_j softmax_j(a_i) v_j with a_ij = scale * q_i . k_j (masked → -inf),
@@ -103,7 +137,8 @@ def attention_fwd(q, k, v, softmax_scale: float, causal: bool = False, row_block
     LSE_i = m_i + log l_i.  ``row_block`` only bounds memory: rows are
     independent, each row is still computed over all of its keys at once.
     ``visible`` (bool [Nq, Nk], optional) masks further keys, e.g. a block-
-    sparse mask from :func:`block_sparse_visible`.
+    sparse mask from :func:`block_sparse_visible`. ``score_mod`` replaces a_ij
+    by its modification (:func:`score_mod_apply`) before the mask.
 
     Returns (O [Nq, d_v], LSE [Nq]) in fp64.
     """
@@ -114,7 +149,7 @@ def attention_fwd(q, k, v, softmax_scale: float, causal: bool = False, row_block
     if nq == 0 or nk == 0:
         return o, lse
     for rows in _row_blocks(nq, row_block):
-        a = _logits(q, k, softmax_scale, rows, nq, nk, causal, visible)
+        a = _logits(q, k, softmax_scale, rows, nq, nk, causal, visible, score_mod)
         m = a.max(axis=1)
         live = np.isfinite(m)
         if not live.any():
@@ -126,11 +161,13 @@ def attention_fwd(q, k, v, softmax_scale: float, causal: bool = False, row_block
     return o, lse
 
 
-def attention_bwd(q, k, v, do, softmax_scale: float, causal: bool = False, row_block=None, visible=None):
+def attention_bwd(q, k, v, do, softmax_scale: float, causal: bool = False, row_block=None, visible=None,
+                  score_mod=None):
     """Dense definition of one head's backward pass for the loss <O, dO>.
 
     P_ij = exp(a_ij - LSE_i); dV_j = sum_i P_ij dO_i; dP_ij = dO_i . v_j;
-    D_i = sum_j P_ij dP_ij; dS_ij = P_ij (dP_ij - D_i);
+    D_i = sum_j P_ij dP_ij; dS_ij = P_ij (dP_ij - D_i) * a'_ij, a' the derivative
+    of the score modification (1 without one);
     dQ_i = scale * sum_j dS_ij k_j; dK_j = scale * sum_i dS_ij q_i.
     ``visible`` masks further keys as in :func:`attention_fwd` (P_ij = 0 there).
 
@@ -146,7 +183,7 @@ def attention_bwd(q, k, v, do, softmax_scale: float, causal: bool = False, row_b
     if nq == 0 or nk == 0:
         return {"dq": dq, "dk": dk, "dv": dv, "D": D}
     for rows in _row_blocks(nq, row_block):
-        a = _logits(q, k, softmax_scale, rows, nq, nk, causal, visible)
+        a, da = _logits(q, k, softmax_scale, rows, nq, nk, causal, visible, score_mod, with_deriv=True)
         m = a.max(axis=1)
         live = np.isfinite(m)
         if not live.any():
@@ -158,7 +195,7 @@ def attention_bwd(q, k, v, do, softmax_scale: float, causal: bool = False, row_b
         dv += p.T @ do[rl]
         dp = do[rl] @ v.T
         d_row = (p * dp).sum(axis=1)
-        ds = p * (dp - d_row[:, None])
+        ds = p * (dp - d_row[:, None]) * da[live]
         dq[rl] = softmax_scale * (ds @ k)
         dk += softmax_scale * (ds.T @ q[rl])
         D[rl] = d_row
@@ -231,14 +268,22 @@ def _seq_bounds(cu):
     return list(zip(cu[:-1], cu[1:]))
 
 
+def head_score_mod(score_mod, h: int):
+    """The score modification of head h: ALiBi takes a per-head slope list."""
+    if score_mod is None or score_mod[0] != "alibi" or np.ndim(score_mod[1]) == 0:
+        return score_mod
+    return ("alibi", float(np.asarray(score_mod[1]).reshape(-1)[h]))
+
+
 def attention_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, softmax_scale: float, causal: bool = False,
-                         seqs=None, heads=None, row_block=None):
+                         seqs=None, heads=None, row_block=None, score_mod=None):
     """Variable-length packed batch: q [total_q, H, d_qk], k/v [total_k, H, d].
 
     Each sequence s attends only within itself (rows cu_q[s]:cu_q[s+1] against
     keys cu_k[s]:cu_k[s+1]), each head independently. ``seqs`` / ``heads``
-    select a subset (others are left as NaN). Returns (O [total_q, H, d_v],
-    LSE [H, total_q]).
+    select a subset (others are left as NaN). ``score_mod`` as in
+    :func:`score_mod_apply`, positions counted within each sequence; ALiBi may
+    give one slope per head. Returns (O [total_q, H, d_v], LSE [H, total_q]).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     tq, H = q.shape[0], q.shape[1]
@@ -248,14 +293,15 @@ def attention_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, softmax_scale: flo
     for s in (range(len(bq)) if seqs is None else seqs):
         (q0, q1), (k0, k1) = bq[s], bk[s]
         for h in (range(H) if heads is None else heads):
-            oo, ll = attention_fwd(q[q0:q1, h], k[k0:k1, h], v[k0:k1, h], softmax_scale, causal, row_block)
+            oo, ll = attention_fwd(q[q0:q1, h], k[k0:k1, h], v[k0:k1, h], softmax_scale, causal, row_block,
+                                   score_mod=head_score_mod(score_mod, h))
             o[q0:q1, h] = oo
             lse[h, q0:q1] = ll
     return o, lse
 
 
 def attention_bwd_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, softmax_scale: float, causal: bool = False,
-                         seqs=None, heads=None, row_block=None):
+                         seqs=None, heads=None, row_block=None, score_mod=None):
     """Backward of :func:`attention_fwd_varlen`; returns (dq, dk, dv) packed (NaN outside the subset)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     dq = np.full(q.shape, np.nan)
@@ -267,7 +313,7 @@ def attention_bwd_varlen(q, k, v, do, cu_seqlens_q, cu_seqlens_k, softmax_scale:
         (q0, q1), (k0, k1) = bq[s], bk[s]
         for h in (range(H) if heads is None else heads):
             g = attention_bwd(q[q0:q1, h], k[k0:k1, h], v[k0:k1, h], do[q0:q1, h], softmax_scale, causal,
-                              row_block)
+                              row_block, score_mod=head_score_mod(score_mod, h))
             dq[q0:q1, h] = g["dq"]
             dk[k0:k1, h] = g["dk"]
             dv[k0:k1, h] = g["dv"]
