@@ -79,6 +79,22 @@ def _fill_fwd(p: AttnFwdParams, q, k, v, o, lse, strides, scale, causal):
     p.causal = 1 if causal else 0
 
 
+def _set_score_mod(p: AttnFwdParams, q: torch.Tensor, softcap, alibi_slopes):
+    """Score modification: logits soft-capped at ``softcap`` (a' = c tanh(a / c)), or ALiBi with one
+    slope per head (``alibi_slopes`` float32 [H] on q's GPU, each >= 0)."""
+    if softcap is not None and alibi_slopes is not None:
+        raise ValueError("choose one score modification: softcap or alibi_slopes")
+    if softcap is not None:
+        p.score_mod, p.softcap = _abi.SCORE_SOFTCAP, float(softcap)
+    elif alibi_slopes is not None:
+        t = alibi_slopes
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.shape != (q.shape[-2],):
+            raise ValueError(f"alibi_slopes must be a contiguous float32 CUDA tensor of shape [{q.shape[-2]}]")
+        if t.device != q.device:
+            raise ValueError(f"alibi_slopes is on {t.device} but q is on {q.device}")
+        p.score_mod, p.alibi_slopes = _abi.SCORE_ALIBI, _ptr(t)
+
+
 def _workspace(size: int, device) -> Tuple[Optional[torch.Tensor], int]:
     if size == 0:
         return None, 0
@@ -88,10 +104,12 @@ def _workspace(size: int, device) -> Tuple[Optional[torch.Tensor], int]:
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = False,
              softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
              lse: Optional[torch.Tensor] = None, rescale_stats: Optional[torch.Tensor] = None,
-             exp2_emu_period: int = 0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+             exp2_emu_period: int = 0, softcap: Optional[float] = None,
+             alibi_slopes: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Dense forward. q [B, Nq, H, d_qk], k [B, Nk, H, d_qk], v [B, Nk, H, d_v] (bf16, CUDA).
     Returns (O [B, Nq, H, d_v] bf16, LSE [B, H, Nq] fp32, natural log). ``exp2_emu_period`` (0, 4, 8)
-    sends one column in that many of every row's exp2 to the FMA-pipe polynomial."""
+    sends one column in that many of every row's exp2 to the FMA-pipe polynomial. ``softcap`` or
+    ``alibi_slopes`` select a score modification (include/attn.h, attn_fwd_params.score_mod)."""
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_bf16(n, t, 4)
     B, Nq, H, dqk = q.shape
@@ -111,41 +129,57 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool 
     p.batch, p.seqlen_q, p.seqlen_k = B, Nq, Nk
     p.rescale_stats = _ptr(rescale_stats)
     p.exp2_emu_period = int(exp2_emu_period)
+    _set_score_mod(p, q, softcap, alibi_slopes)
     ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_fwd(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_fwd")
     return out, lse
 
 
-def _check_lists(q: torch.Tensor, kv_count: torch.Tensor, kv_index: torch.Tensor):
+def _check_lists(q: torch.Tensor, kv_count: torch.Tensor, kv_index: torch.Tensor) -> Tuple[int, int]:
+    """Validates the block lists of a dense [B, Nq, H, d] call; returns (max_kv, lists_per_head).
+    Shared lists: kv_count [nqb], kv_index [nqb, max_kv]. Per (batch, head): kv_count [B, H, nqb],
+    kv_index [B, H, nqb, max_kv]."""
     for n, t in (("kv_count", kv_count), ("kv_index", kv_index)):
         if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
         if t.device != q.device:
             raise ValueError(f"{n} is on {t.device} but q is on {q.device}: the block lists must be on q's GPU")
+    B, Nq, H = q.shape[0], q.shape[1], q.shape[2]
+    nqb = (Nq + 255) // 256
+    if kv_count.shape == (nqb,) and kv_index.dim() == 2 and kv_index.shape[0] == nqb:
+        return int(kv_index.shape[1]), 0
+    if kv_count.shape == (B, H, nqb) and kv_index.dim() == 4 and kv_index.shape[:3] == (B, H, nqb):
+        return int(kv_index.shape[3]), 1
+    raise ValueError(f"kv_count must be [{nqb}] and kv_index [{nqb}, max_kv], or per (batch, head) "
+                     f"[{B}, {H}, {nqb}] and [{B}, {H}, {nqb}, max_kv]")
 
 
 def block_lists_from_mask(block_mask: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
     """(kv_count, kv_index) for :func:`attn_fwd_block_sparse` from a boolean block mask
-    [ceil(Nq/256), ceil(Nk/128)] (True = the query block attends to the key block), key blocks in
-    ascending order; on the mask's device. Argument preparation only."""
-    if block_mask.dtype != torch.bool or block_mask.dim() != 2:
-        raise ValueError("block_mask must be a 2-D bool tensor [query blocks, key blocks]")
+    [ceil(Nq/256), ceil(Nk/128)], or [B, H, ceil(Nq/256), ceil(Nk/128)] for lists per (batch, head)
+    (True = the query block attends to the key block), key blocks in ascending order; on the mask's
+    device. Argument preparation only."""
+    if block_mask.dtype != torch.bool or block_mask.dim() not in (2, 4):
+        raise ValueError("block_mask must be a bool tensor [query blocks, key blocks] or [B, H, query blocks, "
+                         "key blocks]")
     m = block_mask.to(torch.int32)
-    kv_count = m.sum(dim=1, dtype=torch.int32)
+    kv_count = m.sum(dim=-1, dtype=torch.int32)
     max_kv = max(int(kv_count.max().item()) if kv_count.numel() else 0, 1)
     # stable sort puts listed blocks first, each group in ascending key-block order
-    order = torch.sort(1 - m, dim=1, stable=True).indices.to(torch.int32)
-    kv_index = order[:, :max_kv].contiguous()
+    order = torch.sort(1 - m, dim=-1, stable=True).indices.to(torch.int32)
+    kv_index = order[..., :max_kv].contiguous()
     return kv_count.contiguous(), kv_index
 
 
 def attn_fwd_block_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_count: torch.Tensor,
                           kv_index: torch.Tensor, *, causal: bool = False, softmax_scale: Optional[float] = None,
                           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                          softcap: Optional[float] = None, alibi_slopes: Optional[torch.Tensor] = None,
                           stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Block-sparse dense forward. q/k/v as in :func:`attn_fwd`; kv_count int32 [ceil(Nq/256)] and
     kv_index int32 [ceil(Nq/256), max_kv] (CUDA, contiguous): query block b (rows 256b..256b+255)
-    attends to key blocks (of 128 keys) kv_index[b, :kv_count[b]], each listed at most once.
+    attends to key blocks (of 128 keys) kv_index[b, :kv_count[b]], each listed at most once; or per
+    (batch, head), kv_count [B, H, nqb] and kv_index [B, H, nqb, max_kv].
     Returns (O [B, Nq, H, d_v] bf16, LSE [B, H, Nq] fp32)."""
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_bf16(n, t, 4)
@@ -153,10 +187,7 @@ def attn_fwd_block_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_
     Nk, dv = k.shape[1], v.shape[-1]
     if k.shape != (B, Nk, H, dqk) or v.shape[:3] != (B, Nk, H):
         raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
-    nqb = (Nq + 255) // 256
-    _check_lists(q, kv_count, kv_index)
-    if kv_count.shape != (nqb,) or kv_index.dim() != 2 or kv_index.shape[0] != nqb:
-        raise ValueError(f"kv_count must be [{nqb}] and kv_index [{nqb}, max_kv]")
+    max_kv, per_head = _check_lists(q, kv_count, kv_index)
     scale = float(softmax_scale) if softmax_scale is not None else 1.0 / math.sqrt(dqk)
     if out is None:
         out = torch.empty((B, Nq, H, dv), dtype=torch.bfloat16, device=q.device)
@@ -168,8 +199,9 @@ def attn_fwd_block_sparse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_
     p = AttnFwdParams()
     _fill_fwd(p, q, k, v, out, lse, _strides4, scale, causal)
     p.batch, p.seqlen_q, p.seqlen_k = B, Nq, Nk
+    _set_score_mod(p, q, softcap, alibi_slopes)
     ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
-    _abi.check(_lib.attn_fwd_block_sparse(ctypes.byref(p), _ptr(kv_count), _ptr(kv_index), int(kv_index.shape[1]),
+    _abi.check(_lib.attn_fwd_block_sparse(ctypes.byref(p), _ptr(kv_count), _ptr(kv_index), max_kv, per_head,
                                           _ptr(ws), nbytes, _stream(stream)), "attn_fwd_block_sparse")
     return out, lse
 
@@ -178,9 +210,11 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                     cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, *, causal: bool = False,
                     softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                     lse: Optional[torch.Tensor] = None, rescale_stats: Optional[torch.Tensor] = None,
-                    exp2_emu_period: int = 0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                    exp2_emu_period: int = 0, softcap: Optional[float] = None,
+                    alibi_slopes: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Packed variable-length forward. q [total_q, H, d_qk], k/v [total_k, H, d]; cu_seqlens int32 on
-    the device. Returns (O [total_q, H, d_v], LSE [H, total_q])."""
+    the device. Returns (O [total_q, H, d_v], LSE [H, total_q]). Score modifications as in
+    :func:`attn_fwd`, positions counted within each sequence."""
     for n, t in (("q", q), ("k", k), ("v", v)):
         _check_bf16(n, t, 3)
     for n, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
@@ -202,6 +236,7 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
     p.batch = 1
     p.rescale_stats = _ptr(rescale_stats)
     p.exp2_emu_period = int(exp2_emu_period)
+    _set_score_mod(p, q, softcap, alibi_slopes)
     ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_fwd_varlen(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_fwd_varlen")
     return out, lse
@@ -233,10 +268,11 @@ def _event_handles(events):
 
 def attn_bwd(q, k, v, out, lse, dout, *, causal: bool = False, softmax_scale: Optional[float] = None,
              deterministic: bool = False, dq=None, dk=None, dv=None, stream=None, phase_events=None,
-             cta_pair: bool = False):
+             cta_pair: bool = False, softcap: Optional[float] = None, alibi_slopes: Optional[torch.Tensor] = None):
     """Dense backward: returns (dQ, dK, dV) bf16 for the loss <O, dO>. ``phase_events`` (optional, three
     torch.cuda.Event) are recorded after the D pass, the dK/dV kernel and the dQ kernel. ``cta_pair``
-    selects the two-SM (cta_group::2) dK/dV kernel (d = 128)."""
+    selects the two-SM (cta_group::2) dK/dV kernel (d = 128). The score modification must be the
+    forward's."""
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
         _check_bf16(n, t, 4)
     B, Nq, H, dqk = q.shape
@@ -249,6 +285,7 @@ def attn_bwd(q, k, v, out, lse, dout, *, causal: bool = False, softmax_scale: Op
     _fill_fwd(p.fwd, q, k, v, out, lse, _strides4, scale, causal)
     p.fwd.batch, p.fwd.seqlen_q, p.fwd.seqlen_k = B, Nq, Nk
     _fill_bwd(p, dout, dq, dk, dv, _strides4, deterministic, cta_pair)
+    _set_score_mod(p.fwd, q, softcap, alibi_slopes)
     handles = _event_handles(phase_events)
     if handles is not None:
         for i, h in enumerate(handles):
@@ -260,17 +297,15 @@ def attn_bwd(q, k, v, out, lse, dout, *, causal: bool = False, softmax_scale: Op
 
 def attn_bwd_block_sparse(q, k, v, out, lse, dout, kv_count, kv_index, *, causal: bool = False,
                           softmax_scale: Optional[float] = None, deterministic: bool = False, dq=None, dk=None,
-                          dv=None, stream=None):
+                          dv=None, softcap: Optional[float] = None, alibi_slopes: Optional[torch.Tensor] = None,
+                          stream=None):
     """Block-sparse backward for :func:`attn_fwd_block_sparse` with the same kv_count / kv_index:
     returns (dQ, dK, dV) bf16 for the loss <O, dO>."""
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
         _check_bf16(n, t, 4)
     B, Nq, H, dqk = q.shape
     Nk = k.shape[1]
-    nqb = (Nq + 255) // 256
-    _check_lists(q, kv_count, kv_index)
-    if kv_count.shape != (nqb,) or kv_index.dim() != 2 or kv_index.shape[0] != nqb:
-        raise ValueError(f"kv_count must be [{nqb}] and kv_index [{nqb}, max_kv]")
+    max_kv, per_head = _check_lists(q, kv_count, kv_index)
     scale = float(softmax_scale) if softmax_scale is not None else 1.0 / math.sqrt(dqk)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -279,15 +314,17 @@ def attn_bwd_block_sparse(q, k, v, out, lse, dout, kv_count, kv_index, *, causal
     _fill_fwd(p.fwd, q, k, v, out, lse, _strides4, scale, causal)
     p.fwd.batch, p.fwd.seqlen_q, p.fwd.seqlen_k = B, Nq, Nk
     _fill_bwd(p, dout, dq, dk, dv, _strides4, deterministic)
-    ws, nbytes = _workspace(_lib.attn_bwd_block_sparse_workspace_size(ctypes.byref(p)), q.device)
-    _abi.check(_lib.attn_bwd_block_sparse(ctypes.byref(p), _ptr(kv_count), _ptr(kv_index), int(kv_index.shape[1]),
+    _set_score_mod(p.fwd, q, softcap, alibi_slopes)
+    ws, nbytes = _workspace(_lib.attn_bwd_block_sparse_workspace_size(ctypes.byref(p), per_head), q.device)
+    _abi.check(_lib.attn_bwd_block_sparse(ctypes.byref(p), _ptr(kv_count), _ptr(kv_index), max_kv, per_head,
                                           _ptr(ws), nbytes, _stream(stream)), "attn_bwd_block_sparse")
     return dq, dk, dv
 
 
 def attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int, *,
                     causal: bool = False, softmax_scale: Optional[float] = None, deterministic: bool = False,
-                    dq=None, dk=None, dv=None, stream=None, cta_pair: bool = False):
+                    dq=None, dk=None, dv=None, stream=None, cta_pair: bool = False, softcap: Optional[float] = None,
+                    alibi_slopes: Optional[torch.Tensor] = None):
     """Packed variable-length backward: returns (dQ, dK, dV) packed like q, k, v."""
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
         _check_bf16(n, t, 3)
@@ -304,6 +341,7 @@ def attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seq
     p.fwd.total_q, p.fwd.total_k = tq, k.shape[0]
     p.fwd.batch = 1
     _fill_bwd(p, dout, dq, dk, dv, _strides3, deterministic, cta_pair)
+    _set_score_mod(p.fwd, q, softcap, alibi_slopes)
     ws, nbytes = _workspace(_lib.attn_bwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_bwd_varlen(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_bwd_varlen")
     return dq, dk, dv
@@ -329,14 +367,17 @@ def attn_get_device_status(stream=None) -> int:
 
 class _Attention(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, causal, softmax_scale, deterministic, kv_count, kv_index):
+    def forward(ctx, q, k, v, causal, softmax_scale, deterministic, kv_count, kv_index, softcap, alibi_slopes):
+        mod = dict(softcap=softcap, alibi_slopes=alibi_slopes)
         if kv_count is None:
-            o, lse = attn_fwd(q, k, v, causal=causal, softmax_scale=softmax_scale)
+            o, lse = attn_fwd(q, k, v, causal=causal, softmax_scale=softmax_scale, **mod)
         else:
-            o, lse = attn_fwd_block_sparse(q, k, v, kv_count, kv_index, causal=causal, softmax_scale=softmax_scale)
+            o, lse = attn_fwd_block_sparse(q, k, v, kv_count, kv_index, causal=causal, softmax_scale=softmax_scale,
+                                           **mod)
         ctx.save_for_backward(q, k, v, o, lse)
         ctx.causal, ctx.scale, ctx.det = causal, softmax_scale, deterministic
         ctx.lists = (kv_count, kv_index)
+        ctx.mod = mod
         return o
 
     @staticmethod
@@ -345,16 +386,19 @@ class _Attention(torch.autograd.Function):
         kv_count, kv_index = ctx.lists
         if kv_count is None:
             dq, dk, dv = attn_bwd(q, k, v, o, lse, do.contiguous(), causal=ctx.causal, softmax_scale=ctx.scale,
-                                  deterministic=ctx.det)
+                                  deterministic=ctx.det, **ctx.mod)
         else:
             dq, dk, dv = attn_bwd_block_sparse(q, k, v, o, lse, do.contiguous(), kv_count, kv_index,
-                                               causal=ctx.causal, softmax_scale=ctx.scale, deterministic=ctx.det)
-        return dq, dk, dv, None, None, None, None, None
+                                               causal=ctx.causal, softmax_scale=ctx.scale, deterministic=ctx.det,
+                                               **ctx.mod)
+        return dq, dk, dv, None, None, None, None, None, None, None
 
 
 def attention(q, k, v, causal: bool = False, softmax_scale: Optional[float] = None, deterministic: bool = False,
-              block_mask: Optional[Tuple[torch.Tensor, torch.Tensor]] = None):
+              block_mask: Optional[Tuple[torch.Tensor, torch.Tensor]] = None, softcap: Optional[float] = None,
+              alibi_slopes: Optional[torch.Tensor] = None):
     """Autograd wrapper over attn_fwd / attn_bwd for [B, N, H, d] bf16 tensors. ``block_mask``
-    = (kv_count, kv_index) selects the block-sparse pair attn_fwd_block_sparse / attn_bwd_block_sparse."""
+    = (kv_count, kv_index) selects the block-sparse pair attn_fwd_block_sparse / attn_bwd_block_sparse;
+    ``softcap`` / ``alibi_slopes`` a score modification."""
     kv_count, kv_index = block_mask if block_mask is not None else (None, None)
-    return _Attention.apply(q, k, v, causal, softmax_scale, deterministic, kv_count, kv_index)
+    return _Attention.apply(q, k, v, causal, softmax_scale, deterministic, kv_count, kv_index, softcap, alibi_slopes)

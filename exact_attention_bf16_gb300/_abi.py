@@ -10,7 +10,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libattn_gb300.so")
 HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "attn.h")
 
-ABI_VERSION = 2
+ABI_VERSION = 3
 BWD_NOALLOC_SCRATCH_BYTES = 8 << 20  # ATTN_BWD_NOALLOC_SCRATCH_BYTES
 
 STATUS = {
@@ -22,6 +22,7 @@ STATUS = {
     5: "ATTN_ERR_WORKSPACE",
 }
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT, ATTN_ERR_WORKSPACE = range(6)
+SCORE_NONE, SCORE_SOFTCAP, SCORE_ALIBI = range(3)  # attn_score_mod_t
 
 c_i32, c_i64, c_f32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 
@@ -40,6 +41,7 @@ class AttnFwdParams(ctypes.Structure):
         ("total_q", c_i32), ("total_k", c_i32),
         ("softmax_scale", c_f32), ("causal", c_i32), ("exp2_emu_period", c_i32),
         ("rescale_stats", c_vp),
+        ("score_mod", c_i32), ("softcap", ctypes.c_float), ("alibi_slopes", c_vp),
     ]
 
 
@@ -75,10 +77,10 @@ def load(path: str = LIB_PATH):
         "attn_bwd_workspace_size": (ctypes.c_size_t, [P(AttnBwdParams)]),
         "attn_fwd": (ctypes.c_int, [P(AttnFwdParams), c_vp, ctypes.c_size_t, c_vp]),
         "attn_fwd_varlen": (ctypes.c_int, [P(AttnFwdParams), c_vp, ctypes.c_size_t, c_vp]),
-        "attn_fwd_block_sparse": (ctypes.c_int, [P(AttnFwdParams), c_vp, c_vp, ctypes.c_int32, c_vp, ctypes.c_size_t,
-                                                 c_vp]),
-        "attn_bwd_block_sparse_workspace_size": (ctypes.c_size_t, [P(AttnBwdParams)]),
-        "attn_bwd_block_sparse": (ctypes.c_int, [P(AttnBwdParams), c_vp, c_vp, ctypes.c_int32, c_vp,
+        "attn_fwd_block_sparse": (ctypes.c_int, [P(AttnFwdParams), c_vp, c_vp, ctypes.c_int32, ctypes.c_int32, c_vp,
+                                                 ctypes.c_size_t, c_vp]),
+        "attn_bwd_block_sparse_workspace_size": (ctypes.c_size_t, [P(AttnBwdParams), ctypes.c_int32]),
+        "attn_bwd_block_sparse": (ctypes.c_int, [P(AttnBwdParams), c_vp, c_vp, ctypes.c_int32, ctypes.c_int32, c_vp,
                                                  ctypes.c_size_t, c_vp]),
         "attn_bwd": (ctypes.c_int, [P(AttnBwdParams), c_vp, ctypes.c_size_t, c_vp]),
         "attn_bwd_varlen": (ctypes.c_int, [P(AttnBwdParams), c_vp, ctypes.c_size_t, c_vp]),

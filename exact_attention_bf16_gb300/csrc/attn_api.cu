@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "../../include/attn.h"
@@ -197,18 +198,42 @@ attn_status_t check_fwd(const attn_fwd_params* p, bool varlen) {
   ATTN_TRY(check_tensor(p->v, p->v_batch_stride, p->v_row_stride, p->v_head_stride, varlen, ek));
   ATTN_TRY(check_tensor(p->o, p->o_batch_stride, p->o_row_stride, p->o_head_stride, varlen, eq));
   if ((!p->lse && !eq) || (reinterpret_cast<uintptr_t>(p->lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  switch (p->score_mod) {
+    case ATTN_SCORE_NONE: break;
+    case ATTN_SCORE_SOFTCAP:
+      if (!(std::isfinite(p->softcap) && p->softcap > 0.f && std::isfinite(p->softcap / p->softmax_scale)))
+        return ATTN_ERR_INVALID_ARG;
+      break;
+    case ATTN_SCORE_ALIBI:
+      if (!p->alibi_slopes || (reinterpret_cast<uintptr_t>(p->alibi_slopes) & 3u)) return ATTN_ERR_INVALID_ARG;
+      break;
+    default: return ATTN_ERR_INVALID_ARG;
+  }
   return ATTN_OK;
 }
 
-// The block lists must be device memory on the same GPU as the data: a list
-// on another GPU would be read across devices by the kernels.
-attn_status_t check_lists_device(const void* data, const int32_t* kv_count, const int32_t* kv_index) {
+// Score-modification constants for the kernels (score_mod.cuh).
+template <typename Args>
+void fill_score_mod(Args& a, const attn_fwd_params* p) {
+  a.score_mod = p->score_mod;
+  a.inv_scale = 1.f / p->softmax_scale;
+  a.alibi_slopes = p->score_mod == ATTN_SCORE_ALIBI ? p->alibi_slopes : nullptr;
+  if (p->score_mod == ATTN_SCORE_SOFTCAP) {
+    a.mod_k2 = 2.f * 1.4426950408889634f * (p->softmax_scale / p->softcap);
+    a.mod_b = p->softcap / p->softmax_scale;
+  }
+}
+
+// Arrays the kernels read besides the tensors (block lists, ALiBi slopes)
+// must be device memory on the same GPU as the data: one on another GPU would
+// be read across devices.
+attn_status_t check_lists_device(const void* data, std::initializer_list<const void*> arrays) {
   if (!data) return ATTN_OK;  // no rows: nothing is launched
-  cudaPointerAttributes ad{}, ac{}, ai{};
+  cudaPointerAttributes ad{};
   if (cudaPointerGetAttributes(&ad, data) != cudaSuccess) return ATTN_ERR_INVALID_ARG;
-  for (const int32_t* p : {kv_count, kv_index}) {
+  for (const void* p : arrays) {
     if (!p) continue;
-    cudaPointerAttributes& at = p == kv_count ? ac : ai;
+    cudaPointerAttributes at{};
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) return ATTN_ERR_INVALID_ARG;
     if ((at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) || at.device != ad.device)
       return ATTN_ERR_INVALID_ARG;
@@ -221,6 +246,7 @@ struct SparseSpec {
   const int32_t* kv_count = nullptr;
   const int32_t* kv_index = nullptr;
   int32_t max_kv = 0;
+  int32_t lists_per_head = 0;
 };
 
 // Tile list of a packed variable-length launch (launch_tile_list): one
@@ -272,11 +298,13 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
                       const SparseSpec& sp = {}, uint32_t diag_limit = 0) {
   ATTN_TRY(check_fwd(p, varlen));
   if (p->exp2_emu_period != 0 && p->exp2_emu_period != 4 && p->exp2_emu_period != 8) return ATTN_ERR_INVALID_ARG;
+  if (p->score_mod != ATTN_SCORE_NONE && (p->exp2_emu_period != 0 || diag_limit)) return ATTN_ERR_UNSUPPORTED;
   const int nq_rows = varlen ? p->total_q : p->seqlen_q;
   const int nk_rows = varlen ? p->total_k : p->seqlen_k;
   const int units = varlen ? p->num_seqs : p->batch;
   const int max_q = varlen ? p->max_seqlen_q : p->seqlen_q;
   if (nq_rows == 0 || max_q == 0) return ATTN_OK;
+  if (nk_rows > 0 && p->score_mod == ATTN_SCORE_ALIBI) ATTN_TRY(check_lists_device(p->q, {p->alibi_slopes}));
   const size_t need_ws = diag_limit ? 0 : fwd_workspace_bytes(p, varlen);
   if (nk_rows > 0 && need_ws > 0 && (ws == nullptr || ws_bytes < need_ws || (reinterpret_cast<uintptr_t>(ws) & 255u)))
     return ATTN_ERR_WORKSPACE;
@@ -309,7 +337,9 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
   a.kv_count = sp.kv_count;
   a.kv_index = sp.kv_index;
   a.max_kv = sp.max_kv;
+  a.lists_per_head = sp.lists_per_head;
   a.spin_limit = diag_limit;
+  fill_score_mod(a, p);
   cudaError_t e = status_ptr(&a.status);
   if (e != cudaSuccess) return cuda_fail(e, "status word");
 
@@ -396,9 +426,13 @@ size_t bwd_workspace_bytes(const attn_bwd_params* p, bool varlen) {
 }
 
 // Extra workspace of the block-sparse backward: the transposed lists
-// (int32 q_count[n_kb], then q_index[n_kb][n_qb256]) after the D vector.
-size_t bwd_sparse_extra_bytes(const attn_fwd_params& f) {
-  const int64_t n_kb = (static_cast<int64_t>(f.seqlen_k) + 127) / 128;
+// (int32 q_count[sets][n_kb], then q_index[sets][n_kb][n_qb256]) after the D
+// vector; sets = batch * heads for lists per (batch, head), else 1.
+int64_t list_sets(const attn_fwd_params& f, int32_t lists_per_head) {
+  return lists_per_head ? static_cast<int64_t>(f.batch) * f.heads : 1;
+}
+size_t bwd_sparse_extra_bytes(const attn_fwd_params& f, int32_t lists_per_head) {
+  const int64_t n_kb = (static_cast<int64_t>(f.seqlen_k) + 127) / 128 * list_sets(f, lists_per_head);
   const int64_t n_qb = (static_cast<int64_t>(f.seqlen_q) + 255) / 256;
   return static_cast<size_t>((n_kb * 4 + 255) / 256 * 256 + (n_kb * n_qb * 4 + 255) / 256 * 256);
 }
@@ -413,7 +447,8 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
   ATTN_TRY(check_tensor(p->dq, p->dq_batch_stride, p->dq_row_stride, p->dq_head_stride, varlen, eq));
   ATTN_TRY(check_tensor(p->dk, p->dk_batch_stride, p->dk_row_stride, p->dk_head_stride, varlen, ek));
   ATTN_TRY(check_tensor(p->dv, p->dv_batch_stride, p->dv_row_stride, p->dv_head_stride, varlen, ek));
-  if (p->cta_pair && (f.d_qk != 128 || f.d_v != 128 || sp.kv_count)) return ATTN_ERR_UNSUPPORTED;
+  if (p->cta_pair && (f.d_qk != 128 || f.d_v != 128 || sp.kv_count || f.score_mod != ATTN_SCORE_NONE))
+    return ATTN_ERR_UNSUPPORTED;
   const int nq_rows = varlen ? f.total_q : f.seqlen_q;
   const int nk_rows = varlen ? f.total_k : f.seqlen_k;
   if (nq_rows == 0 && nk_rows == 0) return ATTN_OK;
@@ -423,7 +458,8 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
     if (be != cudaSuccess) return be == cudaErrorInvalidDevicePointer ? ATTN_ERR_INVALID_ARG : cuda_fail(be, "device");
   }
   const size_t need_d = bwd_workspace_bytes(p, varlen);
-  const size_t need = need_d + (sp.kv_count ? bwd_sparse_extra_bytes(f) : 0);
+  const size_t need = need_d + (sp.kv_count ? bwd_sparse_extra_bytes(f, sp.lists_per_head) : 0);
+  if (nq_rows > 0 && nk_rows > 0 && f.score_mod == ATTN_SCORE_ALIBI) ATTN_TRY(check_lists_device(f.q, {f.alibi_slopes}));
   if (nq_rows > 0 && nk_rows > 0 && (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u)))
     return ATTN_ERR_WORKSPACE;
 
@@ -457,15 +493,18 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
   a.scale = f.softmax_scale;
   a.scale_log2 = f.softmax_scale * 1.4426950408889634f;
   a.causal = f.causal ? 1 : 0;
+  fill_score_mod(a, &f);
   const int n_kb_sparse = (f.seqlen_k + 127) / 128;
   if (sp.kv_count) {
     a.kv_count = sp.kv_count;
     a.kv_index = sp.kv_index;
     a.max_kv = sp.max_kv;
     a.n_qb256 = (f.seqlen_q + 255) / 256;
+    a.lists_per_head = sp.lists_per_head;
+    const int64_t n_kb_all = static_cast<int64_t>(n_kb_sparse) * list_sets(f, sp.lists_per_head);
     uint8_t* extra = static_cast<uint8_t*>(ws) + need_d;
     a.q_count = reinterpret_cast<int*>(extra);
-    a.q_index = reinterpret_cast<int*>(extra + (static_cast<size_t>(n_kb_sparse) * 4 + 255) / 256 * 256);
+    a.q_index = reinterpret_cast<int*>(extra + (static_cast<size_t>(n_kb_all) * 4 + 255) / 256 * 256);
   }
   cudaError_t e = status_ptr(&a.status);
   if (e != cudaSuccess) return cuda_fail(e, "status word");
@@ -557,45 +596,50 @@ attn_status_t attn_fwd_varlen(const attn_fwd_params* p, void* workspace, size_t 
   return run_fwd(p, true, static_cast<cudaStream_t>(stream), workspace, workspace_bytes);
 }
 
-attn_status_t attn_fwd_block_sparse(const attn_fwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
-                                    int32_t max_kv, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
-  ATTN_TRY(check_fwd(p, false));
-  if (p->exp2_emu_period != 0) return ATTN_ERR_INVALID_ARG;
-  const int64_t n_qblk = (static_cast<int64_t>(p->seqlen_q) + 255) / 256;
+// Shared checks of the block lists; fills `sp`.
+attn_status_t check_block_lists(const attn_fwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
+                                int32_t max_kv, int32_t lists_per_head, bool backward, SparseSpec* sp) {
+  if (lists_per_head != 0 && lists_per_head != 1) return ATTN_ERR_INVALID_ARG;
+  const int64_t sets = list_sets(*p, lists_per_head);
+  const int64_t n_qblk = (static_cast<int64_t>(p->seqlen_q) + 255) / 256 * sets;
+  const int64_t n_kblk = (static_cast<int64_t>(p->seqlen_k) + 127) / 128 * sets;
   if (max_kv < 0 || n_qblk * max_kv > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
+  if (backward && n_kblk * ((static_cast<int64_t>(p->seqlen_q) + 255) / 256) > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
   if (n_qblk > 0) {
     if (!kv_count || (reinterpret_cast<uintptr_t>(kv_count) & 3u)) return ATTN_ERR_INVALID_ARG;
     if (max_kv > 0 && (!kv_index || (reinterpret_cast<uintptr_t>(kv_index) & 3u))) return ATTN_ERR_INVALID_ARG;
+    ATTN_TRY(check_lists_device(p->q, {kv_count, max_kv > 0 ? kv_index : nullptr}));
   }
-  if (n_qblk > 0) ATTN_TRY(check_lists_device(p->q, kv_count, max_kv > 0 ? kv_index : nullptr));
+  sp->kv_count = kv_count;
+  sp->kv_index = kv_index;
+  sp->max_kv = max_kv;
+  sp->lists_per_head = lists_per_head;
+  return ATTN_OK;
+}
+
+attn_status_t attn_fwd_block_sparse(const attn_fwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
+                                    int32_t max_kv, int32_t lists_per_head, void* workspace, size_t workspace_bytes,
+                                    attn_stream_t stream) {
+  ATTN_TRY(check_fwd(p, false));
+  if (p->exp2_emu_period != 0) return ATTN_ERR_INVALID_ARG;
   SparseSpec sp;
-  sp.kv_count = kv_count;
-  sp.kv_index = kv_index;
-  sp.max_kv = max_kv;
+  ATTN_TRY(check_block_lists(p, kv_count, kv_index, max_kv, lists_per_head, false, &sp));
   return run_fwd(p, false, static_cast<cudaStream_t>(stream), workspace, workspace_bytes, sp);
 }
 
-size_t attn_bwd_block_sparse_workspace_size(const attn_bwd_params* p) {
-  if (!p || p->fwd.cu_seqlens_q != nullptr) return 0;
-  return bwd_workspace_bytes(p, false) + bwd_sparse_extra_bytes(p->fwd);
+size_t attn_bwd_block_sparse_workspace_size(const attn_bwd_params* p, int32_t lists_per_head) {
+  if (!p || p->fwd.cu_seqlens_q != nullptr || (lists_per_head != 0 && lists_per_head != 1)) return 0;
+  if (p->fwd.batch < 0 || p->fwd.heads < 0 || p->fwd.seqlen_q < 0 || p->fwd.seqlen_k < 0) return 0;
+  return bwd_workspace_bytes(p, false) + bwd_sparse_extra_bytes(p->fwd, lists_per_head);
 }
 
 attn_status_t attn_bwd_block_sparse(const attn_bwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
-                                    int32_t max_kv, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+                                    int32_t max_kv, int32_t lists_per_head, void* workspace, size_t workspace_bytes,
+                                    attn_stream_t stream) {
   if (!p) return ATTN_ERR_INVALID_ARG;
   ATTN_TRY(check_fwd(&p->fwd, false));
-  const int64_t n_qblk = (static_cast<int64_t>(p->fwd.seqlen_q) + 255) / 256;
-  const int64_t n_kblk = (static_cast<int64_t>(p->fwd.seqlen_k) + 127) / 128;
-  if (max_kv < 0 || n_qblk * max_kv > 0x7fffffff || n_qblk * n_kblk > 0x7fffffff) return ATTN_ERR_INVALID_ARG;
-  if (n_qblk > 0) {
-    if (!kv_count || (reinterpret_cast<uintptr_t>(kv_count) & 3u)) return ATTN_ERR_INVALID_ARG;
-    if (max_kv > 0 && (!kv_index || (reinterpret_cast<uintptr_t>(kv_index) & 3u))) return ATTN_ERR_INVALID_ARG;
-  }
-  if (n_qblk > 0) ATTN_TRY(check_lists_device(p->fwd.q, kv_count, max_kv > 0 ? kv_index : nullptr));
   SparseSpec sp;
-  sp.kv_count = kv_count;
-  sp.kv_index = kv_index;
-  sp.max_kv = max_kv;
+  ATTN_TRY(check_block_lists(&p->fwd, kv_count, kv_index, max_kv, lists_per_head, true, &sp));
   return run_bwd(p, workspace, workspace_bytes, false, static_cast<cudaStream_t>(stream), sp);
 }
 

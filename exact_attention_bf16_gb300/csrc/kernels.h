@@ -99,10 +99,22 @@ struct FwdArgs {
   // the number of entries (the grid).
   const TileEntry* tiles;
   int64_t n_tiles;
+  // Score modification (score_mod.cuh): kind, softcap's 2 log2(e) scale / c and
+  // c / scale, 1 / scale for ALiBi's per-head slopes (device float[heads]).
+  int score_mod;
+  float mod_k2, mod_b, inv_scale;
+  const float* alibi_slopes;
+  // Block-sparse: 0 = one list set shared by every (batch, head); 1 = one per
+  // (batch, head), set (b * heads + h) starting at count index (b * heads + h) * n_mblk.
+  int lists_per_head;
 };
 
 cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tv16, const FwdArgs& a, cudaStream_t stream);
+// The forward with a score modification (a.score_mod != 0, emu_period 0):
+// dense, tile list (a.tiles) or block-sparse (a.kv_count), by the arguments.
+cudaError_t launch_fwd_mod(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tv16, const FwdArgs& a, cudaStream_t stream);
 
 // fp16 copy of V (contiguous [nb, nrows, heads, dv]) for the forward's PV
 // product; ORs 1 into *flag (zeroed by the caller) if a finite value is out of
@@ -165,6 +177,13 @@ struct BwdArgs {
   int64_t n_tiles_kv;
   const TileEntry* tiles_q;
   int64_t n_tiles_q;
+  // Score modification, as in FwdArgs.
+  int score_mod;
+  float mod_k2, mod_b, inv_scale;
+  const float* alibi_slopes;
+  // Block-sparse: 1 = lists per (batch, head): forward set (b * heads + h) at
+  // count index (b * heads + h) * n_qb256, transposed set at (b * heads + h) * n_kb.
+  int lists_per_head;
 };
 
 // D = rowsum(dO * O) into args.dsum.
@@ -173,6 +192,12 @@ cudaError_t launch_bwd_preprocess(int d_v, const BwdArgs& a, cudaStream_t stream
 // a.kv_count set they walk the block-sparse lists (dense layout only).
 cudaError_t launch_bwd_dkdv(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+// The dK/dV and dQ kernels with a score modification (a.score_mod != 0),
+// dense, tile list or block-sparse by the arguments.
+cudaError_t launch_bwd_dkdv_mod(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dq_mod(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
 // dK, dV for d_qk = d_v = 128 over CTA pairs (dense or varlen, no block
 // lists): maps q and dO with 64-row boxes (_r) and 128-row boxes (_c), k, v.
 cudaError_t launch_bwd_dkdv_pair(const CUtensorMap& tq_r, const CUtensorMap& tq_c, const CUtensorMap& tk,

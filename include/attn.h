@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 2
+#define ATTN_ABI_VERSION 3
 
 typedef enum {
   ATTN_OK = 0,
@@ -73,6 +73,13 @@ typedef enum {
   ATTN_ERR_TIMEOUT = 4,      /* a kernel's bounded wait gave up (device status word) */
   ATTN_ERR_WORKSPACE = 5     /* workspace missing or smaller than *_workspace_size */
 } attn_status_t;
+
+/* Score modifications (attn_fwd_params.score_mod). */
+typedef enum {
+  ATTN_SCORE_NONE = 0,
+  ATTN_SCORE_SOFTCAP = 1,  /* a' = softcap * tanh(a / softcap) */
+  ATTN_SCORE_ALIBI = 2     /* a' = a - m_h * |j - (i + Nk - Nq)| */
+} attn_score_mod_t;
 
 /* Opaque CUDA stream handle (cudaStream_t); NULL is the legacy default stream. */
 typedef void* attn_stream_t;
@@ -127,6 +134,24 @@ typedef struct attn_fwd_params {
    * the number of conditional rescales performed after a row's first key
    * tile ([0]) and the number of such rescale opportunities ([1]). */
   unsigned long long* rescale_stats;
+  /* Score modification (the FlexAttention variants built on FA4: wittx
+   * "FlashAttention-4", section Python写GPU内核), applied to the scaled logit
+   * a = softmax_scale * q_i . k_j of every visible (query i, key j) before the
+   * softmax, i and j counted within the sequence; LSE is that of the modified
+   * logits and the backward differentiates through the modification:
+   *   ATTN_SCORE_NONE: a unchanged (softcap and alibi_slopes are ignored);
+   *   ATTN_SCORE_SOFTCAP: a' = softcap * tanh(a / softcap), softcap finite and
+   *     > 0 (else ATTN_ERR_INVALID_ARG); the backward multiplies dS by
+   *     1 - tanh^2(a / softcap);
+   *   ATTN_SCORE_ALIBI: a' = a - m_h |j - (i + Nk - Nq)|, m_h = alibi_slopes[h],
+   *     a device float[heads] on q's GPU, 4-byte aligned (else
+   *     ATTN_ERR_INVALID_ARG), each finite and >= 0 (the kernels use |m_h|).
+   * A modification needs exp2_emu_period == 0 and, in the backward,
+   * cta_pair == 0 (else ATTN_ERR_UNSUPPORTED); any other value of score_mod
+   * is ATTN_ERR_INVALID_ARG. */
+  int32_t score_mod;
+  float softcap;
+  const float* alibi_slopes;
 } attn_fwd_params;
 
 /* Backward parameters. `fwd` holds q, k, v, the forward's outputs o and lse
@@ -192,10 +217,15 @@ attn_status_t attn_fwd(const attn_fwd_params* p, void* workspace, size_t workspa
  * exp2_emu_period must be 0. Query rows form blocks of 256 (block b = rows
  * 256b .. 256b+255), keys blocks of 128. Query block b attends to the key
  * blocks kv_index[b * max_kv + j] for j < kv_count[b]; every other key is
- * masked, and `causal` still applies inside the listed blocks. kv_count
- * (int32[ceil(seqlen_q / 256)]) and kv_index (int32[ceil(seqlen_q / 256) *
- * max_kv]) are device arrays owned by the caller, shared by every (batch,
- * head), 4-byte aligned; ceil(seqlen_q / 256) * max_kv < 2^31. Counts are
+ * masked, and `causal` still applies inside the listed blocks. With
+ * lists_per_head == 0 one set of lists serves every (batch, head): kv_count
+ * is int32[nqb] and kv_index int32[nqb * max_kv], nqb = ceil(seqlen_q / 256).
+ * With lists_per_head == 1 each (batch b, head h) has its own set, stored one
+ * after another: kv_count int32[batch * heads * nqb] and kv_index
+ * int32[batch * heads * nqb * max_kv], the set of (b, h) at offsets
+ * (b * heads + h) * nqb and (b * heads + h) * nqb * max_kv; other values are
+ * ATTN_ERR_INVALID_ARG. Both are device arrays owned by the caller, 4-byte
+ * aligned, and hold fewer than 2^31 entries. Counts are
  * clamped to [0, max_kv]; indices outside [0, ceil(seqlen_k / 128)) list
  * nothing. Each key block must be listed at most once per query block: the
  * forward counts a repeated block once per listing, and the backward's result
@@ -204,7 +234,8 @@ attn_status_t attn_fwd(const attn_fwd_params* p, void* workspace, size_t workspa
  * The workspace is that of attn_fwd (attn_fwd_workspace_size). The gradients
  * come from attn_bwd_block_sparse. */
 attn_status_t attn_fwd_block_sparse(const attn_fwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
-                                    int32_t max_kv, void* workspace, size_t workspace_bytes, attn_stream_t stream);
+                                    int32_t max_kv, int32_t lists_per_head, void* workspace, size_t workspace_bytes,
+                                    attn_stream_t stream);
 /* Variable-length forward (cu_seqlens_q / cu_seqlens_k required). */
 attn_status_t attn_fwd_varlen(const attn_fwd_params* p, void* workspace, size_t workspace_bytes,
                               attn_stream_t stream);
@@ -215,14 +246,15 @@ attn_status_t attn_bwd_varlen(const attn_bwd_params* p, void* workspace, size_t 
                               attn_stream_t stream);
 
 /* Block-sparse backward: the gradients of attn_fwd_block_sparse for the same
- * kv_count / kv_index / max_kv (same rules, blocks listed at most once;
- * dense layout only). The lists must be on the same GPU as q. The key
- * blocks' transposed lists are built on the stream into the workspace, whose
- * size is attn_bwd_block_sparse_workspace_size(p) (16-byte aligned). Both
- * modes are bitwise reproducible, as for attn_bwd. */
-size_t attn_bwd_block_sparse_workspace_size(const attn_bwd_params* p);
+ * kv_count / kv_index / max_kv / lists_per_head (same rules, blocks listed at
+ * most once; dense layout only). The lists must be on the same GPU as q. The
+ * key blocks' transposed lists are built on the stream into the workspace,
+ * whose size is attn_bwd_block_sparse_workspace_size(p, lists_per_head)
+ * (16-byte aligned). Both modes are bitwise reproducible, as for attn_bwd. */
+size_t attn_bwd_block_sparse_workspace_size(const attn_bwd_params* p, int32_t lists_per_head);
 attn_status_t attn_bwd_block_sparse(const attn_bwd_params* p, const int32_t* kv_count, const int32_t* kv_index,
-                                    int32_t max_kv, void* workspace, size_t workspace_bytes, attn_stream_t stream);
+                                    int32_t max_kv, int32_t lists_per_head, void* workspace, size_t workspace_bytes,
+                                    attn_stream_t stream);
 
 /* Backward for callers that cannot allocate device memory (an engine that
  * plans all memory up front and forbids later cudaMalloc, a plugin that is

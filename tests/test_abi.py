@@ -141,7 +141,7 @@ def test_block_sparse_rejects_bad_arguments_without_a_gpu(lib, _abi, mutate, exp
     p = _valid_fwd(_abi)
     p.seqlen_q = 600  # three query blocks of 256 rows
     p, (cnt, idx, max_kv) = mutate(p, _valid_sparse_args())
-    assert lib.attn_fwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, None, 0, None) == expect
+    assert lib.attn_fwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, 0, None, 0, None) == expect
 
 
 @pytest.mark.parametrize("mutate,expect", [
@@ -157,7 +157,7 @@ def test_block_sparse_backward_rejects_bad_arguments_without_a_gpu(lib, _abi, mu
     p.fwd = _valid_fwd(_abi)
     p.fwd.seqlen_q = 600
     p, (cnt, idx, max_kv) = mutate(p, _valid_sparse_args())
-    assert lib.attn_bwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, None, 0, None) == expect
+    assert lib.attn_bwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, 0, None, 0, None) == expect
 
 
 def test_block_sparse_backward_workspace_size(lib, _abi):
@@ -165,10 +165,67 @@ def test_block_sparse_backward_workspace_size(lib, _abi):
     p.fwd = _valid_fwd(_abi)
     p.fwd.seqlen_q, p.fwd.seqlen_k = 600, 1000  # 3 query blocks of 256, 8 key blocks of 128
     dense = lib.attn_bwd_workspace_size(ctypes.byref(p))
-    sparse = lib.attn_bwd_block_sparse_workspace_size(ctypes.byref(p))
-    assert sparse >= dense + 8 * 4 + 8 * 3 * 4  # q_count[8] and q_index[8][3] on top of the D vector
+    r256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    sparse = lib.attn_bwd_block_sparse_workspace_size(ctypes.byref(p), 0)
+    assert sparse == dense + r256(8 * 4) + r256(8 * 3 * 4)  # q_count[8] and q_index[8][3] after the D vector
+    per_head = lib.attn_bwd_block_sparse_workspace_size(ctypes.byref(p), 1)  # B1 H4: four sets
+    assert per_head == dense + r256(4 * 8 * 4) + r256(4 * 8 * 3 * 4)
+    assert lib.attn_bwd_block_sparse_workspace_size(ctypes.byref(p), 2) == 0
     p.fwd.cu_seqlens_q = 0x10000
-    assert lib.attn_bwd_block_sparse_workspace_size(ctypes.byref(p)) == 0  # dense layout only
+    assert lib.attn_bwd_block_sparse_workspace_size(ctypes.byref(p), 0) == 0  # dense layout only
+
+
+@pytest.mark.parametrize("lists_per_head,max_kv,expect", [
+    (2, 3, INVALID),                 # neither shared nor per (batch, head)
+    (-1, 3, INVALID),
+    (1, 0x7fffffff // 12 + 1, INVALID),  # B1 H4 x 3 query blocks x max_kv overflows int32
+])
+def test_block_lists_per_head_rejects_bad_arguments_without_a_gpu(lib, _abi, lists_per_head, max_kv, expect):
+    p = _valid_fwd(_abi)
+    p.seqlen_q = 600
+    cnt, idx, _ = _valid_sparse_args()
+    assert lib.attn_fwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, lists_per_head, None, 0, None) == expect
+    b = _abi.AttnBwdParams()
+    b.fwd = p
+    b.dout = b.dq = b.dk = b.dv = 0x10000
+    for t in ("do", "dq", "dk", "dv"):
+        setattr(b, f"{t}_batch_stride", 128 * 4 * 64)
+        setattr(b, f"{t}_row_stride", 4 * 64)
+        setattr(b, f"{t}_head_stride", 64)
+    assert lib.attn_bwd_block_sparse(ctypes.byref(b), cnt, idx, max_kv, lists_per_head, None, 0, None) == expect
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda p: setattr(p, "score_mod", 3), INVALID),                              # unknown modification
+    (lambda p: setattr(p, "score_mod", -1), INVALID),
+    (lambda p: (setattr(p, "score_mod", 1), setattr(p, "softcap", 0.0)), INVALID),   # cap must be > 0
+    (lambda p: (setattr(p, "score_mod", 1), setattr(p, "softcap", -2.0)), INVALID),
+    (lambda p: (setattr(p, "score_mod", 1), setattr(p, "softcap", float("inf"))), INVALID),
+    (lambda p: (setattr(p, "score_mod", 1), setattr(p, "softcap", float("nan"))), INVALID),
+    (lambda p: (setattr(p, "score_mod", 1), setattr(p, "softcap", 3e38)), INVALID),   # cap / scale overflows
+    (lambda p: setattr(p, "score_mod", 2), INVALID),                              # ALiBi without slopes
+    (lambda p: (setattr(p, "score_mod", 2), setattr(p, "alibi_slopes", 0x10002)), INVALID),  # misaligned
+    (lambda p: (setattr(p, "score_mod", 1), setattr(p, "softcap", 30.0),
+                setattr(p, "exp2_emu_period", 8)), UNSUPPORTED),                  # no emulated exp2 with a mod
+])
+def test_score_mod_rejects_bad_arguments_without_a_gpu(lib, _abi, mutate, expect):
+    p = _valid_fwd(_abi)
+    mutate(p)
+    assert lib.attn_fwd(ctypes.byref(p), None, 0, None) == expect
+
+
+def test_score_mod_rejected_with_the_two_sm_backward(lib, _abi):
+    p = _abi.AttnBwdParams()
+    p.fwd = _valid_fwd(_abi)
+    p.fwd.d_qk = p.fwd.d_v = 128
+    p.fwd.score_mod, p.fwd.softcap = 1, 30.0
+    p.dout = p.dq = p.dk = p.dv = 0x10000
+    for t in ("do", "dq", "dk", "dv"):
+        setattr(p, f"{t}_batch_stride", 128 * 4 * 128)
+        setattr(p, f"{t}_row_stride", 4 * 128)
+        setattr(p, f"{t}_head_stride", 128)
+    p.cta_pair = 1
+    assert lib.attn_bwd(ctypes.byref(p), None, 0, None) == UNSUPPORTED
 
 
 @pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++17")])
@@ -236,7 +293,7 @@ def test_cta_pair_backward_only_for_d128_without_lists(lib, _abi):
     assert lib.attn_bwd(ctypes.byref(p), None, 0, None) == _abi.ATTN_ERR_UNSUPPORTED
     p.fwd.d_qk, p.fwd.d_v = 128, 128
     cnt, idx, max_kv = _valid_sparse_args()
-    assert lib.attn_bwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, None, 0, None) in (
+    assert lib.attn_bwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, 0, None, 0, None) in (
         _abi.ATTN_ERR_UNSUPPORTED, _abi.ATTN_ERR_INVALID_ARG)
 
 

@@ -93,6 +93,6 @@ def test_block_lists_on_another_device_are_rejected():
     p.batch, p.seqlen_q, p.seqlen_k = 1, 300, 300
     ws = torch.empty(lib.attn_fwd_workspace_size(ctypes.byref(p)), dtype=torch.uint8, device="cuda")
     st = lib.attn_fwd_block_sparse(ctypes.byref(p), ctypes.c_void_p(cnt.data_ptr()),
-                                   ctypes.c_void_p(idx.data_ptr()), int(idx.shape[1]), ctypes.c_void_p(ws.data_ptr()),
+                                   ctypes.c_void_p(idx.data_ptr()), int(idx.shape[1]), 0, ctypes.c_void_p(ws.data_ptr()),
                                    ws.numel(), None)
     assert st == abi.ATTN_ERR_INVALID_ARG
