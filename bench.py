@@ -236,9 +236,10 @@ def time_ms(fn, stream, reps: int = 5, warm: int = 2) -> float:
 def measure_configs(ea, dev, stream) -> dict:
     """Forward and backward TFLOP/s of every workload the metric covers: the
     d=128 sequence sweep (B*N = 32768, both masks), the outlier variant, the
-    forward with part of exp2 on the FMA pipe, the (192,128) shape, the
-    N=16384 training shape in both backward modes and the 32-sequence varlen
-    batch. Inputs stay resident; each number is a median of 5 launches."""
+    forward with part of exp2 on the FMA pipe, the two score modifications,
+    the (192,128) shape, the N=16384 training shape in both backward modes
+    and the 32-sequence varlen batch. Inputs stay resident; each number is a
+    median of 5 launches."""
     import torch
     import workloads
     out = {}
@@ -251,18 +252,21 @@ def measure_configs(ea, dev, stream) -> dict:
             r.update(bwd_ms=bwd_ms, bwd_tflops=workloads.workload_flops(w, "bwd") / (bwd_ms * 1e-3) / 1e12)
         out[name] = r
 
-    def dense(w, bwd=True, emu=0, modes=(False,)):
+    def dense(w, bwd=True, emu=0, modes=(False,), mod=None):
         t = workloads.make_dense(w, device=dev)
-        o, lse = ea.attn_fwd(t["q"], t["k"], t["v"], causal=w.causal, softmax_scale=w.scale)
+        mod = dict(mod or {})
+        if "alibi_slopes" in mod:
+            mod["alibi_slopes"] = torch.tensor(mod["alibi_slopes"], dtype=torch.float32, device=dev)
+        o, lse = ea.attn_fwd(t["q"], t["k"], t["v"], causal=w.causal, softmax_scale=w.scale, **mod)
         f = time_ms(lambda: ea.attn_fwd(t["q"], t["k"], t["v"], causal=w.causal, softmax_scale=w.scale, out=o,
-                                        lse=lse, exp2_emu_period=emu), stream)
+                                        lse=lse, exp2_emu_period=emu, **mod), stream)
         res = {"fwd": f}
         if bwd:
             g = tuple(torch.empty_like(t[n]) for n in ("q", "k", "v"))
             for det in modes:
                 res[det] = time_ms(lambda: ea.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=w.causal,
                                                        softmax_scale=w.scale, deterministic=det, dq=g[0], dk=g[1],
-                                                       dv=g[2]), stream)
+                                                       dv=g[2], **mod), stream)
         del t, o, lse
         torch.cuda.empty_cache()
         return res
@@ -291,6 +295,13 @@ def measure_configs(ea, dev, stream) -> dict:
         rec(f"dense_d128_B4_N8192_{'causal' if causal else 'noncausal'}_bwd_cta_pair", w, None, b, cta_pair=True)
         del t, o, lse, g
         torch.cuda.empty_cache()
+    for name, mod in (("softcap_30", {"softcap": 30.0}),
+                      ("alibi", {"alibi_slopes": [2.0 ** (-8.0 * (h + 1) / 16) for h in range(16)]})):
+        for causal in (False, True):  # score modifications on the headline shape
+            w = workloads.dense_d128(8192, causal)
+            r = dense(w, mod=mod)
+            rec(f"dense_d128_B4_N8192_{'causal' if causal else 'noncausal'}_{name}", w, r["fwd"], r[False],
+                score_mod=name)
     w = workloads.mla_192_128()
     r = dense(w)
     rec("mla_192_128_B2_H32_N8192_causal", w, r["fwd"], r[False])
