@@ -16,6 +16,7 @@ attention.py  the plain definition of attention (dense softmax-then-matmul),
               the score modifications (logit soft-capping, ALiBi distance bias).
 exp2_poly.py  the Cody-Waite split + degree-3 polynomial exp2 emulation, with
               its own minimax (Remez exchange) coefficient fit.
+fp8.py        FP8 E4M3 codes to values, from the format's definition.
 
 Every function is pinned by tests in ``tests/test_oracle_*.py`` against closed
 forms, invariants, finite differences and hand-worked examples.
@@ -33,3 +34,4 @@ from .attention import (  # noqa: F401
     visible_limit,
 )
 from .exp2_poly import fit_exp2_poly_remez, exp2_poly, exp2_exact  # noqa: F401
+from .fp8 import e4m3_decode  # noqa: F401
