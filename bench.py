@@ -237,7 +237,7 @@ def measure_configs(ea, dev, stream) -> dict:
     """Forward and backward TFLOP/s of every workload the metric covers: the
     d=128 sequence sweep (B*N = 32768, both masks), the outlier variant, the
     forward with part of exp2 on the FMA pipe, the two score modifications,
-    the (192,128) shape, the N=16384 training shape in both backward modes
+    the forward on FP8 E4M3 inputs, the (192,128) shape, the N=16384 training shape in both backward modes
     and the 32-sequence varlen batch. Inputs stay resident; each number is a
     median of 5 launches."""
     import torch
@@ -302,6 +302,20 @@ def measure_configs(ea, dev, stream) -> dict:
             r = dense(w, mod=mod)
             rec(f"dense_d128_B4_N8192_{'causal' if causal else 'noncausal'}_{name}", w, r["fwd"], r[False],
                 score_mod=name)
+    for causal in (False, True):  # FP8 E4M3 inputs (forward only): S on the 8-bit tensor-core kind
+        w = workloads.dense_d128(8192, causal)
+        t = workloads.make_dense(w, device=dev, with_do=False)
+        f8, ds = {}, {}
+        for n in ("q", "k", "v"):
+            ds[n] = float(t[n].abs().max()) / 448.0
+            f8[n] = (t[n].float() / ds[n]).to(torch.float8_e4m3fn)
+        del t
+        kw = dict(causal=causal, softmax_scale=w.scale, q_descale=ds["q"], k_descale=ds["k"], v_descale=ds["v"])
+        o, lse = ea.attn_fwd(f8["q"], f8["k"], f8["v"], **kw)
+        f = time_ms(lambda: ea.attn_fwd(f8["q"], f8["k"], f8["v"], out=o, lse=lse, **kw), stream)
+        rec(f"dense_d128_B4_N8192_{'causal' if causal else 'noncausal'}_e4m3_inputs", w, f, input_dtype="e4m3")
+        del f8, o, lse
+        torch.cuda.empty_cache()
     w = workloads.mla_192_128()
     r = dense(w)
     rec("mla_192_128_B2_H32_N8192_causal", w, r["fwd"], r[False])

@@ -57,6 +57,26 @@ def _check_bf16(name: str, t: torch.Tensor, ndim: int):
         raise ValueError(f"{name}: head_dim must be contiguous")
 
 
+def _check_inputs(q, k, v, ndim: int) -> bool:
+    """q, k, v all bf16, or all FP8 E4M3 (torch.float8_e4m3fn, forward only); returns True for E4M3."""
+    f8 = q.dtype == torch.float8_e4m3fn
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        if f8:
+            if not isinstance(t, torch.Tensor) or t.dtype != torch.float8_e4m3fn:
+                raise TypeError(f"{n} must be float8_e4m3fn like q")
+            if not t.is_cuda or t.dim() != ndim or t.stride(-1) != 1:
+                raise ValueError(f"{n} must be a CUDA tensor of {ndim} dims with contiguous head_dim")
+        else:
+            _check_bf16(n, t, ndim)
+    return f8
+
+
+def _set_input_dtype(p: AttnFwdParams, f8: bool, q_descale, k_descale, v_descale):
+    if f8:
+        p.input_dtype = _abi.INPUT_E4M3
+        p.q_descale, p.k_descale, p.v_descale = float(q_descale), float(k_descale), float(v_descale)
+
+
 def _strides4(t: torch.Tensor):
     # [B, N, H, d] -> (batch, row, head) element strides
     return t.stride(0), t.stride(1), t.stride(2)
@@ -105,13 +125,15 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool 
              softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
              lse: Optional[torch.Tensor] = None, rescale_stats: Optional[torch.Tensor] = None,
              exp2_emu_period: int = 0, softcap: Optional[float] = None,
-             alibi_slopes: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+             alibi_slopes: Optional[torch.Tensor] = None, q_descale: float = 1.0, k_descale: float = 1.0,
+             v_descale: float = 1.0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Dense forward. q [B, Nq, H, d_qk], k [B, Nk, H, d_qk], v [B, Nk, H, d_v] (bf16, CUDA).
     Returns (O [B, Nq, H, d_v] bf16, LSE [B, H, Nq] fp32, natural log). ``exp2_emu_period`` (0, 4, 8)
     sends one column in that many of every row's exp2 to the FMA-pipe polynomial. ``softcap`` or
-    ``alibi_slopes`` select a score modification (include/attn.h, attn_fwd_params.score_mod)."""
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _check_bf16(n, t, 4)
+    ``alibi_slopes`` select a score modification (include/attn.h, attn_fwd_params.score_mod).
+    q, k, v may instead all be torch.float8_e4m3fn (d = 128), standing for their values times
+    ``q_descale``, ``k_descale``, ``v_descale``."""
+    f8 = _check_inputs(q, k, v, 4)
     B, Nq, H, dqk = q.shape
     Nk, dv = k.shape[1], v.shape[-1]
     if k.shape != (B, Nk, H, dqk) or v.shape[:3] != (B, Nk, H):
@@ -130,6 +152,7 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool 
     p.rescale_stats = _ptr(rescale_stats)
     p.exp2_emu_period = int(exp2_emu_period)
     _set_score_mod(p, q, softcap, alibi_slopes)
+    _set_input_dtype(p, f8, q_descale, k_descale, v_descale)
     ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_fwd(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_fwd")
     return out, lse
@@ -211,12 +234,12 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                     softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                     lse: Optional[torch.Tensor] = None, rescale_stats: Optional[torch.Tensor] = None,
                     exp2_emu_period: int = 0, softcap: Optional[float] = None,
-                    alibi_slopes: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                    alibi_slopes: Optional[torch.Tensor] = None, q_descale: float = 1.0, k_descale: float = 1.0,
+                    v_descale: float = 1.0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Packed variable-length forward. q [total_q, H, d_qk], k/v [total_k, H, d]; cu_seqlens int32 on
-    the device. Returns (O [total_q, H, d_v], LSE [H, total_q]). Score modifications as in
-    :func:`attn_fwd`, positions counted within each sequence."""
-    for n, t in (("q", q), ("k", k), ("v", v)):
-        _check_bf16(n, t, 3)
+    the device. Returns (O [total_q, H, d_v], LSE [H, total_q]). Score modifications and E4M3 inputs
+    as in :func:`attn_fwd`, positions counted within each sequence."""
+    f8 = _check_inputs(q, k, v, 3)
     for n, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
         if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
@@ -237,6 +260,7 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
     p.rescale_stats = _ptr(rescale_stats)
     p.exp2_emu_period = int(exp2_emu_period)
     _set_score_mod(p, q, softcap, alibi_slopes)
+    _set_input_dtype(p, f8, q_descale, k_descale, v_descale)
     ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_fwd_varlen(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_fwd_varlen")
     return out, lse

@@ -23,6 +23,7 @@ STATUS = {
 }
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT, ATTN_ERR_WORKSPACE = range(6)
 SCORE_NONE, SCORE_SOFTCAP, SCORE_ALIBI = range(3)  # attn_score_mod_t
+INPUT_BF16, INPUT_E4M3 = range(2)  # attn_input_dtype_t
 
 c_i32, c_i64, c_f32, c_vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 
@@ -42,6 +43,8 @@ class AttnFwdParams(ctypes.Structure):
         ("softmax_scale", c_f32), ("causal", c_i32), ("exp2_emu_period", c_i32),
         ("rescale_stats", c_vp),
         ("score_mod", c_i32), ("softcap", ctypes.c_float), ("alibi_slopes", c_vp),
+        ("input_dtype", c_i32), ("q_descale", ctypes.c_float), ("k_descale", ctypes.c_float),
+        ("v_descale", ctypes.c_float),
     ]
 
 

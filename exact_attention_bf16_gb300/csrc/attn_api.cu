@@ -68,8 +68,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // strides (sb, sn, sh) and unit stride on d. Box: 64 columns x 1 head x
 // `box_rows` rows x 1 batch, 128-byte swizzle (the UMMA K-major / MN-major
 // SW128 layout). Out-of-range rows read as zero.
+// elem_bytes 2: bf16 / fp16 elements, 64-column boxes; 1: E4M3 bytes, 128-column
+// boxes. Either way a box row is one 128-byte swizzled chunk.
 attn_status_t make_map(CUtensorMap* m, const void* base, int d, int n_heads, int64_t n_rows, int n_b, int64_t sb,
-                       int64_t sn, int64_t sh, int box_rows) {
+                       int64_t sn, int64_t sh, int box_rows, int elem_bytes = 2) {
   auto enc = encode_fn();
   if (!enc) return cuda_fail(cudaErrorNotSupported, "cuTensorMapEncodeTiled unavailable");
   // Size-1 dimensions may carry any stride; give them a valid one.
@@ -77,11 +79,13 @@ attn_status_t make_map(CUtensorMap* m, const void* base, int d, int n_heads, int
   if (n_b == 1) sb = sn * (n_rows > 0 ? n_rows : 1);
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n_heads),
                         static_cast<cuuint64_t>(n_rows > 0 ? n_rows : 1), static_cast<cuuint64_t>(n_b)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(sh) * 2, static_cast<cuuint64_t>(sn) * 2,
-                           static_cast<cuuint64_t>(sb) * 2};
-  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint64_t eb = static_cast<cuuint64_t>(elem_bytes);
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(sh) * eb, static_cast<cuuint64_t>(sn) * eb,
+                           static_cast<cuuint64_t>(sb) * eb};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elem_bytes), 1, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+  const CUtensorMapDataType ty = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(m, ty, 4, const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -299,6 +303,22 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
   ATTN_TRY(check_fwd(p, varlen));
   if (p->exp2_emu_period != 0 && p->exp2_emu_period != 4 && p->exp2_emu_period != 8) return ATTN_ERR_INVALID_ARG;
   if (p->score_mod != ATTN_SCORE_NONE && (p->exp2_emu_period != 0 || diag_limit)) return ATTN_ERR_UNSUPPORTED;
+  const bool f8 = p->input_dtype == ATTN_INPUT_E4M3;
+  if (f8) {
+    if (p->d_qk != 128 || p->d_v != 128 || p->exp2_emu_period != 0 || p->score_mod != ATTN_SCORE_NONE ||
+        sp.kv_count != nullptr || diag_limit)
+      return ATTN_ERR_UNSUPPORTED;
+    for (float dsc : {p->q_descale, p->k_descale, p->v_descale})
+      if (!(std::isfinite(dsc) && dsc > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(p->softmax_scale * p->q_descale * p->k_descale)) return ATTN_ERR_INVALID_ARG;
+    for (int64_t st : {p->q_row_stride, p->q_head_stride, p->k_row_stride, p->k_head_stride, p->v_row_stride,
+                       p->v_head_stride})
+      if (st % 16) return ATTN_ERR_INVALID_ARG;  // TMA strides: multiples of 16 bytes
+    if (!varlen && (p->q_batch_stride % 16 || p->k_batch_stride % 16 || p->v_batch_stride % 16))
+      return ATTN_ERR_INVALID_ARG;
+  } else if (p->input_dtype != ATTN_INPUT_BF16) {
+    return ATTN_ERR_INVALID_ARG;
+  }
   const int nq_rows = varlen ? p->total_q : p->seqlen_q;
   const int nk_rows = varlen ? p->total_k : p->seqlen_k;
   const int units = varlen ? p->num_seqs : p->batch;
@@ -331,6 +351,11 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
   a.num_units = units;
   a.n_mblk = (max_q + 255) / 256;
   a.scale_log2 = p->softmax_scale * 1.4426950408889634f;
+  if (f8) {  // S of the codes times both descales
+    a.scale_log2 = p->softmax_scale * p->q_descale * p->k_descale * 1.4426950408889634f;
+    a.input_e4m3 = 1;
+    a.v_descale = p->v_descale;
+  }
   a.causal = p->causal ? 1 : 0;
   a.stats = p->rescale_stats;
   a.emu_period = p->exp2_emu_period;
@@ -357,12 +382,13 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
 
   const int nb = varlen ? 1 : p->batch;
   CUtensorMap tq, tk, tv;
+  const int eb = f8 ? 1 : 2;
   ATTN_TRY(make_map(&tq, p->q, p->d_qk, p->heads, nq_rows, nb, p->q_batch_stride, p->q_row_stride,
-                    p->q_head_stride, 128));
+                    p->q_head_stride, 128, eb));
   ATTN_TRY(make_map(&tk, p->k, p->d_qk, p->heads, nk_rows, nb, p->k_batch_stride, p->k_row_stride,
-                    p->k_head_stride, 128));
+                    p->k_head_stride, 128, eb));
   ATTN_TRY(make_map(&tv, p->v, p->d_v, p->heads, nk_rows, nb, p->v_batch_stride, p->v_row_stride,
-                    p->v_head_stride, 128));
+                    p->v_head_stride, 128, eb));
   if (diag_limit) {
     e = launch_fwd_diag_timeout(tq, tk, tv, a, stream);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "fwd diag launch");
@@ -375,7 +401,10 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
   ATTN_TRY(make_map(&tv16, v16, p->d_v, p->heads, nk_rows, nb, v16_rows * p->heads * p->d_v,
                     static_cast<int64_t>(p->heads) * p->d_v, p->d_v, 128));
   e = cudaMemsetAsync(flag, 0, sizeof(uint32_t), stream);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess && f8)  // exact: every E4M3 value is an fp16 value, the flag stays 0
+    e = launch_v_e4m3_to_f16(p->v, varlen ? 0 : p->v_batch_stride, p->v_row_stride, p->v_head_stride, nb, nk_rows,
+                             p->heads, p->d_v, v16, stream);
+  else if (e == cudaSuccess)
     e = launch_v_to_f16(p->v, varlen ? 0 : p->v_batch_stride, p->v_row_stride, p->v_head_stride, nb, nk_rows,
                         p->heads, p->d_v, v16, flag, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fwd V conversion");
@@ -391,8 +420,9 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
     a.tiles = list;
     a.n_tiles = lp.bound;
   }
-  e = sp.kv_count ? launch_fwd_sparse(p->d_qk, p->d_v, tq, tk, tv, tv16, a, stream)
-                  : launch_fwd(p->d_qk, p->d_v, tq, tk, tv, tv16, a, stream);
+  if (f8) e = launch_fwd_e4m3(tq, tk, tv16, a, stream);
+  else if (sp.kv_count) e = launch_fwd_sparse(p->d_qk, p->d_v, tq, tk, tv, tv16, a, stream);
+  else e = launch_fwd(p->d_qk, p->d_v, tq, tk, tv, tv16, a, stream);
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "fwd launch");
 }
 
@@ -449,6 +479,8 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
   ATTN_TRY(check_tensor(p->dv, p->dv_batch_stride, p->dv_row_stride, p->dv_head_stride, varlen, ek));
   if (p->cta_pair && (f.d_qk != 128 || f.d_v != 128 || sp.kv_count || f.score_mod != ATTN_SCORE_NONE))
     return ATTN_ERR_UNSUPPORTED;
+  if (f.input_dtype != ATTN_INPUT_BF16)  // E4M3 is a forward-only input type
+    return f.input_dtype == ATTN_INPUT_E4M3 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
   const int nq_rows = varlen ? f.total_q : f.seqlen_q;
   const int nk_rows = varlen ? f.total_k : f.seqlen_k;
   if (nq_rows == 0 && nk_rows == 0) return ATTN_OK;
@@ -622,6 +654,8 @@ attn_status_t attn_fwd_block_sparse(const attn_fwd_params* p, const int32_t* kv_
                                     attn_stream_t stream) {
   ATTN_TRY(check_fwd(p, false));
   if (p->exp2_emu_period != 0) return ATTN_ERR_INVALID_ARG;
+  if (p->input_dtype != ATTN_INPUT_BF16)  // E4M3 inputs: dense and varlen forward only
+    return p->input_dtype == ATTN_INPUT_E4M3 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
   SparseSpec sp;
   ATTN_TRY(check_block_lists(p, kv_count, kv_index, max_kv, lists_per_head, false, &sp));
   return run_fwd(p, false, static_cast<cudaStream_t>(stream), workspace, workspace_bytes, sp);

@@ -57,9 +57,12 @@ constexpr float kThreshold = 8.0f;  // log2 units (factor 256)
 __host__ __device__ constexpr uint32_t tS(int i) { return 128u * i; }
 __host__ __device__ constexpr uint32_t tO(int i) { return 256u + 128u * i; }
 
-template <int DQK, int DV>
+// F8: Q and K are E4M3 bytes, so a 128-byte swizzled chunk holds 128 columns
+// instead of 64 (V is always the fp16 copy or bf16: 64 columns per chunk).
+template <int DQK, int DV, bool F8 = false>
 struct Cfg {
-  static constexpr int QCH = DQK / 64;  // 64-column chunks of Q/K
+  static constexpr int QX = F8 ? 128 : 64;  // Q/K columns per 128-byte chunk
+  static constexpr int QCH = DQK / QX;      // 128-byte chunks of a Q/K row
   static constexpr int VCH = DV / 64;
   static constexpr int Q_BYTES = QCH * kChunk;
   static constexpr int K_BYTES = QCH * kChunk;
@@ -117,12 +120,18 @@ __device__ __forceinline__ int key_limit(int row, int nq, int nk, int causal) {
 //
 // MOD: the score modification (score_mod.cuh) applied to every raw logit of a
 // tile before the mask and the row max; 0 for none.
-template <int DQK, int DV, int EMU_PERIOD, bool SPARSE = false, bool DIAG = false, bool LIST = false, int MOD = 0>
+//
+// F8: Q and K are FP8 E4M3 and S = Q K^T runs as tcgen05 kind::f8f6f4 (32
+// columns per k-step, the same 32 bytes of each swizzled row as a bf16 k-step);
+// their descale factors are folded into a.scale_log2 by the host, V is the
+// exact fp16 copy and O is multiplied by a.v_descale in the epilogue.
+template <int DQK, int DV, int EMU_PERIOD, bool SPARSE = false, bool DIAG = false, bool LIST = false, int MOD = 0,
+          bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmv16,
                     const FwdArgs a) {
-  using C = Cfg<DQK, DV>;
+  using C = Cfg<DQK, DV, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -228,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < QT; ++i) {
         mbar_arrive_expect_tx(&bar->q_full[i], C::Q_BYTES);
         for (int c = 0; c < C::QCH; ++c)
-          tma_load_4d(sQ + i * C::Q_BYTES + c * kChunk, &tmq, &bar->q_full[i], c * 64, h, q_start + row0 + i * BM, b);
+          tma_load_4d(sQ + i * C::Q_BYTES + c * kChunk, &tmq, &bar->q_full[i], c * C::QX, h, q_start + row0 + i * BM, b);
       }
       // read while the Q copies fly: V from the fp16 copy, or the bf16 original
       const CUtensorMap* tmvv = v_is_f16(a) ? &tmv16 : &tmv;
@@ -247,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (which == 0) {
             mbar_arrive_expect_tx(&bar->kv_full[slot], C::K_BYTES);
             for (int c = 0; c < C::QCH; ++c)
-              tma_load_4d(dst + c * kChunk, &tmk, &bar->kv_full[slot], c * 64, h, k_start + kb * BN, b);
+              tma_load_4d(dst + c * kChunk, &tmk, &bar->kv_full[slot], c * C::QX, h, k_start + kb * BN, b);
           } else {
             mbar_arrive_expect_tx(&bar->kv_full[slot], C::V_BYTES);
             for (int c = 0; c < C::VCH; ++c)
@@ -267,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ======================= MMA issuer =====================================
     if (lane == 0) {
-      constexpr uint32_t idS = idesc_bf16_f32(BM, BN, false, false);
+      constexpr uint32_t idS = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, false, false);
       const uint32_t idO = v_is_f16(a) ? idesc_f16_f32(BM, DV, false, true) : idesc_bf16_f32(BM, DV, false, true);
       bool ok = mbar_wait(&bar->q_full[0], 0, a.status, 0x200, poll_lim) &&
                 mbar_wait(&bar->q_full[1], 0, a.status, 0x201, poll_lim);
@@ -303,9 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // S_i = Q_i K_j^T, both K-major, 16-wide k-steps walking the 128-byte swizzle atoms
             const uint64_t dq = smem_desc(smem_u32(sQ + i * C::Q_BYTES), 16, 1024, SWZ_128B);
 #pragma unroll
-            for (int kk = 0; kk < DQK / 16; ++kk) {
+            for (int kk = 0; kk < C::QCH * 4; ++kk) {  // 32-byte k-steps of the swizzled rows
               const uint32_t off = (kk / 4) * kChunk + (kk % 4) * 32;
-              mma_ss(tbase + tS(i), desc_add(dq, off), desc_add(dk, off), idS, kk > 0 ? 1u : 0u);
+              if constexpr (F8) mma_ss_f8(tbase + tS(i), desc_add(dq, off), desc_add(dk, off), idS, kk > 0 ? 1u : 0u);
+              else mma_ss(tbase + tS(i), desc_add(dq, off), desc_add(dk, off), idS, kk > 0 ? 1u : 0u);
             }
             mma_commit(&bar->s_full[i]);
           }
@@ -444,7 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait_warp(&bar->o_full[i], 0, a.status, 0x310 + i, poll_lim);
       tc_fence_after();
     }
-    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    if constexpr (F8) inv_l *= a.v_descale;
     __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) + static_cast<int64_t>(b) * a.o_sb +
                           static_cast<int64_t>(q_start + row) * a.o_sn + static_cast<int64_t>(h) * a.o_sh;
     const bool store = row < nq;
@@ -481,11 +492,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-template <int DQK, int DV, int EMU, bool SPARSE = false, bool DIAG = false, bool LIST = false, int MOD = 0>
+template <int DQK, int DV, int EMU, bool SPARSE = false, bool DIAG = false, bool LIST = false, int MOD = 0,
+          bool F8 = false>
 cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tv16,
                      const FwdArgs& a, cudaStream_t stream) {
-  using C = Cfg<DQK, DV>;
-  auto kern = attn_fwd_kernel<DQK, DV, EMU, SPARSE, DIAG, LIST, MOD>;
+  using C = Cfg<DQK, DV, F8>;
+  auto kern = attn_fwd_kernel<DQK, DV, EMU, SPARSE, DIAG, LIST, MOD, F8>;
   static PerDeviceOnce once;
   cudaError_t e = once.run([&]() -> cudaError_t {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -497,7 +509,8 @@ cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     return fa.numRegs * kThreads < C::REG_BUDGET ? cudaErrorInvalidConfiguration : cudaSuccess;
   });
   if (e != cudaSuccess) return e;
-  if (LIST != (a.tiles != nullptr) || MOD != a.score_mod || SPARSE != (a.kv_count != nullptr))
+  if (LIST != (a.tiles != nullptr) || MOD != a.score_mod || SPARSE != (a.kv_count != nullptr) ||
+      F8 != (a.input_e4m3 != 0))
     return cudaErrorInvalidValue;
   const int64_t grid = LIST ? a.n_tiles : static_cast<int64_t>(a.n_mblk) * a.num_units * a.heads;
   if (grid <= 0) return cudaSuccess;

@@ -107,10 +107,20 @@ struct FwdArgs {
   // Block-sparse: 0 = one list set shared by every (batch, head); 1 = one per
   // (batch, head), set (b * heads + h) starting at count index (b * heads + h) * n_mblk.
   int lists_per_head;
+  // E4M3 inputs (maps tq, tk over bytes; V read from its fp16 copy): O is
+  // multiplied by v_descale (Q's and K's descales are in scale_log2).
+  int input_e4m3;
+  float v_descale;
 };
 
 cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tv16, const FwdArgs& a, cudaStream_t stream);
+// The forward with E4M3 Q, K, V (d_qk = d_v = 128, dense or tile list).
+cudaError_t launch_fwd_e4m3(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv16, const FwdArgs& a,
+                            cudaStream_t stream);
+// fp16 copy of E4M3 V (exact), laid out as launch_v_to_f16's.
+cudaError_t launch_v_e4m3_to_f16(const void* v, int64_t sb, int64_t sn, int64_t sh, int nb, int nrows, int heads,
+                                 int dv, void* out, cudaStream_t stream);
 // The forward with a score modification (a.score_mod != 0, emu_period 0):
 // dense, tile list (a.tiles) or block-sparse (a.kv_count), by the arguments.
 cudaError_t launch_fwd_mod(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

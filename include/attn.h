@@ -81,6 +81,12 @@ typedef enum {
   ATTN_SCORE_ALIBI = 2     /* a' = a - m_h * |j - (i + Nk - Nq)| */
 } attn_score_mod_t;
 
+/* Element type of q, k, v (attn_fwd_params.input_dtype). */
+typedef enum {
+  ATTN_INPUT_BF16 = 0,
+  ATTN_INPUT_E4M3 = 1  /* FP8 E4M3 codes (1 byte each), with per-tensor descale factors */
+} attn_input_dtype_t;
+
 /* Opaque CUDA stream handle (cudaStream_t); NULL is the legacy default stream. */
 typedef void* attn_stream_t;
 
@@ -152,6 +158,23 @@ typedef struct attn_fwd_params {
   int32_t score_mod;
   float softcap;
   const float* alibi_slopes;
+  /* Element type of q, k and v (the FP8 path of FA3 and the lower precisions
+   * named for later versions: ainexis "Tri Dao FlashAttention-4", 背景; wittx
+   * "FlashAttention-4", closing section). ATTN_INPUT_BF16 (0, the descales are
+   * ignored) or ATTN_INPUT_E4M3 (1): q, k, v hold FP8 E4M3 codes (OCP FP8,
+   * 1 byte per element, bias 7, max 448) standing for code * q_descale,
+   * code * k_descale and code * v_descale; each descale finite and > 0 (else
+   * ATTN_ERR_INVALID_ARG). E4M3 is a forward-only type (attn_fwd and
+   * attn_fwd_varlen) for d_qk = d_v = 128, exp2_emu_period 0 and no score
+   * modification; other uses, the block-sparse forward and every backward
+   * entry point give ATTN_ERR_UNSUPPORTED. Strides (in elements = bytes) must
+   * be multiples of 16. O (bf16) and LSE (fp32) are as for bf16 inputs: the
+   * result of attention on the dequantised values. Other values of
+   * input_dtype are ATTN_ERR_INVALID_ARG. */
+  int32_t input_dtype;
+  float q_descale;
+  float k_descale;
+  float v_descale;
 } attn_fwd_params;
 
 /* Backward parameters. `fwd` holds q, k, v, the forward's outputs o and lse

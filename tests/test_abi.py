@@ -335,3 +335,49 @@ def test_bwd_workspace_size_holds_the_tile_lists(lib, _abi):
     p.cta_pair = 0
     f.cu_seqlens_q = f.cu_seqlens_k = 0  # dense: D only
     assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == r256(4 * 4 * 128)
+
+
+def _valid_fwd_e4m3(_abi):
+    p = _valid_fwd(_abi)
+    p.d_qk = p.d_v = 128
+    for t in "qkvo":
+        setattr(p, f"{t}_batch_stride", 128 * 4 * 128)
+        setattr(p, f"{t}_row_stride", 4 * 128)
+        setattr(p, f"{t}_head_stride", 128)
+    p.input_dtype, p.q_descale, p.k_descale, p.v_descale = 1, 0.01, 0.02, 0.03
+    return p
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda p: setattr(p, "input_dtype", 2), INVALID),                   # unknown element type
+    (lambda p: setattr(p, "q_descale", 0.0), INVALID),                   # descales finite and > 0
+    (lambda p: setattr(p, "k_descale", -1.0), INVALID),
+    (lambda p: setattr(p, "v_descale", float("nan")), INVALID),
+    (lambda p: setattr(p, "v_descale", float("inf")), INVALID),
+    (lambda p: setattr(p, "q_row_stride", 4 * 128 + 8), INVALID),        # byte strides: multiples of 16
+    (lambda p: setattr(p, "k_head_stride", 136), INVALID),
+    (lambda p: (setattr(p, "d_qk", 64), setattr(p, "d_v", 64)), UNSUPPORTED),  # d = 128 only
+    (lambda p: setattr(p, "exp2_emu_period", 8), UNSUPPORTED),
+    (lambda p: (setattr(p, "score_mod", 1), setattr(p, "softcap", 30.0)), UNSUPPORTED),
+])
+def test_e4m3_forward_rejects_bad_arguments_without_a_gpu(lib, _abi, mutate, expect):
+    p = _valid_fwd_e4m3(_abi)
+    mutate(p)
+    assert lib.attn_fwd(ctypes.byref(p), None, 0, None) == expect
+
+
+def test_e4m3_is_forward_only(lib, _abi):
+    p = _valid_fwd_e4m3(_abi)
+    p.seqlen_q = 600
+    cnt, idx, max_kv = _valid_sparse_args()
+    assert lib.attn_fwd_block_sparse(ctypes.byref(p), cnt, idx, max_kv, 0, None, 0, None) == UNSUPPORTED
+    b = _abi.AttnBwdParams()
+    b.fwd = _valid_fwd_e4m3(_abi)
+    b.dout = b.dq = b.dk = b.dv = 0x10000
+    for t in ("do", "dq", "dk", "dv"):
+        setattr(b, f"{t}_batch_stride", 128 * 4 * 128)
+        setattr(b, f"{t}_row_stride", 4 * 128)
+        setattr(b, f"{t}_head_stride", 128)
+    assert lib.attn_bwd(ctypes.byref(b), None, 0, None) == UNSUPPORTED
+    b.fwd.input_dtype = 2
+    assert lib.attn_bwd(ctypes.byref(b), None, 0, None) == INVALID
