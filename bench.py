@@ -237,7 +237,8 @@ def measure_configs(ea, dev, stream) -> dict:
     """Forward and backward TFLOP/s of every workload the metric covers: the
     d=128 sequence sweep (B*N = 32768, both masks), the outlier variant, the
     forward with part of exp2 on the FMA pipe, the two score modifications,
-    the forward on FP8 E4M3 inputs, the (192,128) shape, the N=16384 training shape in both backward modes
+    the forward on FP8 E4M3 inputs, the d=64 backward in its two-kernel and
+    single-pass forms, the (192,128) shape, the N=16384 training shape in both backward modes
     and the 32-sequence varlen batch. Inputs stay resident; each number is a
     median of 5 launches."""
     import torch
@@ -315,6 +316,19 @@ def measure_configs(ea, dev, stream) -> dict:
         f = time_ms(lambda: ea.attn_fwd(f8["q"], f8["k"], f8["v"], out=o, lse=lse, **kw), stream)
         rec(f"dense_d128_B4_N8192_{'causal' if causal else 'noncausal'}_e4m3_inputs", w, f, input_dtype="e4m3")
         del f8, o, lse
+        torch.cuda.empty_cache()
+    for causal in (False, True):  # d = 64: two-kernel backward against the single pass (dQ reduced across CTAs)
+        w = workloads.Workload(f"d64_N8192{'_causal' if causal else ''}", 4, 16, 8192, 8192, 64, 64, causal, seed=0)
+        t = workloads.make_dense(w, device=dev)
+        o, lse = ea.attn_fwd(t["q"], t["k"], t["v"], causal=causal, softmax_scale=w.scale)
+        g = tuple(torch.empty_like(t[n]) for n in ("q", "k", "v"))
+        name = f"dense_d64_B4_H16_N8192_{'causal' if causal else 'noncausal'}"
+        for label, kw in (("two_kernel", {}), ("single_pass", {"single_pass": True}),
+                          ("single_pass_deterministic", {"single_pass": True, "deterministic": True})):
+            b = time_ms(lambda: ea.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=causal,
+                                            softmax_scale=w.scale, dq=g[0], dk=g[1], dv=g[2], **kw), stream)
+            rec(f"{name}_bwd_{label}", w, None, b, backward=label)
+        del t, o, lse, g
         torch.cuda.empty_cache()
     w = workloads.mla_192_128()
     r = dense(w)

@@ -266,7 +266,7 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
     return out, lse
 
 
-def _fill_bwd(p: AttnBwdParams, do, dq, dk, dv, strides, deterministic, cta_pair=False):
+def _fill_bwd(p: AttnBwdParams, do, dq, dk, dv, strides, deterministic, cta_pair=False, single_pass=False):
     p.dout, p.dq, p.dk, p.dv = _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv)
     (p.do_batch_stride, p.do_row_stride, p.do_head_stride) = strides(do)
     (p.dq_batch_stride, p.dq_row_stride, p.dq_head_stride) = strides(dq)
@@ -274,6 +274,7 @@ def _fill_bwd(p: AttnBwdParams, do, dq, dk, dv, strides, deterministic, cta_pair
     (p.dv_batch_stride, p.dv_row_stride, p.dv_head_stride) = strides(dv)
     p.deterministic = 1 if deterministic else 0
     p.cta_pair = 1 if cta_pair else 0
+    p.single_pass = 1 if single_pass else 0
 
 
 def _event_handles(events):
@@ -292,11 +293,13 @@ def _event_handles(events):
 
 def attn_bwd(q, k, v, out, lse, dout, *, causal: bool = False, softmax_scale: Optional[float] = None,
              deterministic: bool = False, dq=None, dk=None, dv=None, stream=None, phase_events=None,
-             cta_pair: bool = False, softcap: Optional[float] = None, alibi_slopes: Optional[torch.Tensor] = None):
+             cta_pair: bool = False, softcap: Optional[float] = None, alibi_slopes: Optional[torch.Tensor] = None,
+             single_pass: bool = False):
     """Dense backward: returns (dQ, dK, dV) bf16 for the loss <O, dO>. ``phase_events`` (optional, three
     torch.cuda.Event) are recorded after the D pass, the dK/dV kernel and the dQ kernel. ``cta_pair``
-    selects the two-SM (cta_group::2) dK/dV kernel (d = 128). The score modification must be the
-    forward's."""
+    selects the two-SM (cta_group::2) dK/dV kernel (d = 128); ``single_pass`` the one-kernel backward
+    whose dQ partials are reduced across CTAs (d = 64; ordered by key tile when ``deterministic``).
+    The score modification must be the forward's."""
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
         _check_bf16(n, t, 4)
     B, Nq, H, dqk = q.shape
@@ -308,7 +311,7 @@ def attn_bwd(q, k, v, out, lse, dout, *, causal: bool = False, softmax_scale: Op
     p = AttnBwdParams()
     _fill_fwd(p.fwd, q, k, v, out, lse, _strides4, scale, causal)
     p.fwd.batch, p.fwd.seqlen_q, p.fwd.seqlen_k = B, Nq, Nk
-    _fill_bwd(p, dout, dq, dk, dv, _strides4, deterministic, cta_pair)
+    _fill_bwd(p, dout, dq, dk, dv, _strides4, deterministic, cta_pair, single_pass)
     _set_score_mod(p.fwd, q, softcap, alibi_slopes)
     handles = _event_handles(phase_events)
     if handles is not None:
@@ -348,7 +351,7 @@ def attn_bwd_block_sparse(q, k, v, out, lse, dout, kv_count, kv_index, *, causal
 def attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int, *,
                     causal: bool = False, softmax_scale: Optional[float] = None, deterministic: bool = False,
                     dq=None, dk=None, dv=None, stream=None, cta_pair: bool = False, softcap: Optional[float] = None,
-                    alibi_slopes: Optional[torch.Tensor] = None):
+                    alibi_slopes: Optional[torch.Tensor] = None, single_pass: bool = False):
     """Packed variable-length backward: returns (dQ, dK, dV) packed like q, k, v."""
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
         _check_bf16(n, t, 3)
@@ -364,7 +367,7 @@ def attn_bwd_varlen(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seq
     p.fwd.max_seqlen_q, p.fwd.max_seqlen_k = int(max_seqlen_q), int(max_seqlen_k)
     p.fwd.total_q, p.fwd.total_k = tq, k.shape[0]
     p.fwd.batch = 1
-    _fill_bwd(p, dout, dq, dk, dv, _strides3, deterministic, cta_pair)
+    _fill_bwd(p, dout, dq, dk, dv, _strides3, deterministic, cta_pair, single_pass)
     _set_score_mod(p.fwd, q, softcap, alibi_slopes)
     ws, nbytes = _workspace(_lib.attn_bwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_bwd_varlen(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_bwd_varlen")

@@ -10,7 +10,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libattn_gb300.so")
 HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "attn.h")
 
-ABI_VERSION = 3
+ABI_VERSION = 4
 BWD_NOALLOC_SCRATCH_BYTES = 8 << 20  # ATTN_BWD_NOALLOC_SCRATCH_BYTES
 
 STATUS = {
@@ -58,6 +58,7 @@ class AttnBwdParams(ctypes.Structure):
         ("dv_batch_stride", c_i64), ("dv_row_stride", c_i64), ("dv_head_stride", c_i64),
         ("deterministic", c_i32), ("cta_pair", c_i32),
         ("phase_events", c_vp * 3),
+        ("single_pass", c_i32),
     ]
 
 

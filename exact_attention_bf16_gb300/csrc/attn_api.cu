@@ -447,12 +447,33 @@ ListPlan bwd_q_plan(const attn_bwd_params* p, bool varlen) {
   const attn_fwd_params& f = p->fwd;
   return varlen ? list_plan(f.total_q, f.num_seqs, f.heads, f.max_seqlen_q, 128) : ListPlan{};
 }
+// Single pass (d = 64): the fp32 dQ buffer, 4 bytes per query row, head and
+// column, then (deterministic) one int32 semaphore per (unit, head, 64-row tile).
+size_t bwd_dq_acc_bytes(const attn_bwd_params* p, bool varlen) {
+  const attn_fwd_params& f = p->fwd;
+  if (!p->single_pass || f.heads < 0 || (varlen ? f.total_q < 0 : (f.batch < 0 || f.seqlen_q < 0))) return 0;
+  const int64_t rows = varlen ? static_cast<int64_t>(f.heads) * f.total_q
+                              : static_cast<int64_t>(f.batch) * f.heads * f.seqlen_q;
+  return round256(rows * f.d_qk * 4);
+}
+int64_t bwd_n_qt64(const attn_bwd_params* p, bool varlen) {
+  const attn_fwd_params& f = p->fwd;
+  return ((varlen ? static_cast<int64_t>(f.max_seqlen_q) : f.seqlen_q) + 63) / 64;
+}
+size_t bwd_sem_bytes(const attn_bwd_params* p, bool varlen) {
+  const attn_fwd_params& f = p->fwd;
+  if (!p->single_pass || !p->deterministic || f.heads < 0) return 0;
+  const int64_t units = varlen ? f.num_seqs : f.batch;
+  if (units < 0 || bwd_n_qt64(p, varlen) < 0) return 0;
+  return round256(units * f.heads * bwd_n_qt64(p, varlen) * 4);
+}
 size_t bwd_workspace_bytes(const attn_bwd_params* p, bool varlen) {
   const size_t d = bwd_d_bytes(p, varlen);
-  if (!varlen) return d;
+  const size_t fused = bwd_dq_acc_bytes(p, varlen) + bwd_sem_bytes(p, varlen);
+  if (!varlen) return d + fused;
   const ListPlan kv = bwd_kv_plan(p, varlen), q = bwd_q_plan(p, varlen);
   const size_t lists = (kv.use ? kv.list_bytes : 0) + (q.use ? q.list_bytes : 0);
-  return d + lists + (lists ? seq_scratch_bytes(p->fwd.num_seqs) : 0);
+  return d + lists + (lists ? seq_scratch_bytes(p->fwd.num_seqs) : 0) + fused;
 }
 
 // Extra workspace of the block-sparse backward: the transposed lists
@@ -481,6 +502,9 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
     return ATTN_ERR_UNSUPPORTED;
   if (f.input_dtype != ATTN_INPUT_BF16)  // E4M3 is a forward-only input type
     return f.input_dtype == ATTN_INPUT_E4M3 ? ATTN_ERR_UNSUPPORTED : ATTN_ERR_INVALID_ARG;
+  if (p->single_pass && (f.d_qk != 64 || f.d_v != 64 || sp.kv_count || f.score_mod != ATTN_SCORE_NONE ||
+                         p->cta_pair))
+    return ATTN_ERR_UNSUPPORTED;
   const int nq_rows = varlen ? f.total_q : f.seqlen_q;
   const int nk_rows = varlen ? f.total_k : f.seqlen_k;
   if (nq_rows == 0 && nk_rows == 0) return ATTN_OK;
@@ -589,6 +613,19 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
   if (e == cudaSuccess && sp.kv_count) e = launch_bwd_transpose_lists(a, n_kb_sparse, stream);
   if (e == cudaSuccess) e = mark(0);
   if (e != cudaSuccess) return cuda_fail(e, "bwd preprocess launch");
+  if (p->single_pass) {  // dK, dV and the dQ partials in one kernel, then dQ * scale to bf16
+    uint8_t* tail = static_cast<uint8_t*>(ws) + bwd_workspace_bytes(p, varlen) - bwd_dq_acc_bytes(p, varlen) -
+                    bwd_sem_bytes(p, varlen);
+    a.dq_acc = reinterpret_cast<float*>(tail);
+    a.dq_sem = p->deterministic ? reinterpret_cast<int*>(tail + bwd_dq_acc_bytes(p, varlen)) : nullptr;
+    a.n_qt64 = static_cast<int>(bwd_n_qt64(p, varlen));
+    e = cudaMemsetAsync(tail, 0, bwd_dq_acc_bytes(p, varlen) + bwd_sem_bytes(p, varlen), stream);
+    if (e == cudaSuccess) e = launch_bwd_single_pass(tq2, tk, tv, tdo2, a, stream);
+    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess) e = launch_bwd_dq_convert(a, f.d_qk, stream);
+    if (e == cudaSuccess) e = mark(2);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "bwd single-pass launch");
+  }
   if (p->cta_pair) {  // the two-SM kernel (d = 128, no block lists; checked before any launch)
     CUtensorMap tq_r, tdo_r;
     ATTN_TRY(make_map(&tq_r, f.q, f.d_qk, f.heads, nq_rows, nb, f.q_batch_stride, f.q_row_stride, f.q_head_stride,

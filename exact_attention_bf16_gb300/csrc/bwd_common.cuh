@@ -22,12 +22,13 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
   for (int t = 0; t < 4; ++t) d[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
 }
 
-// Sequence bounds of a work unit (dense: unit = batch index).
+// Sequence bounds of a work unit (dense: unit = batch index; varlen: b = 0 and
+// unit = the sequence).
 struct Unit {
-  int b, q_start, k_start, nq, nk;
+  int b, q_start, k_start, nq, nk, unit;
 };
 __device__ __forceinline__ Unit unit_bounds(const BwdArgs& a, int unit) {
-  Unit u{unit, 0, 0, a.seqlen_q, a.seqlen_k};
+  Unit u{unit, 0, 0, a.seqlen_q, a.seqlen_k, unit};
   if (a.cu_q != nullptr) {
     u.b = 0;
     u.q_start = a.cu_q[unit];
@@ -49,7 +50,7 @@ __device__ __forceinline__ bool bwd_work(const BwdArgs& a, const TileEntry* tile
     const int4* te = reinterpret_cast<const int4*>(tiles + blockIdx.x);
     const int4 t0 = __ldg(te), t1 = __ldg(te + 1);
     if (t1.z < 0) return false;
-    U = Unit{0, t0.x, t0.z, t0.y, t0.w};
+    U = Unit{0, t0.x, t0.z, t0.y, t0.w, t1.z};
     h = t1.x;
     blk = t1.y;
     return true;

@@ -74,7 +74,14 @@ __device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int chunks
 // soon as the softmax warps have copied this tile's out of TMEM, so the
 // tensor core computes them while the softmax runs. V (and for d_qk = 64 also
 // K) sits in TMEM as an MMA A operand; the rest is read from shared memory.
-template <int DQK, int DV>
+//
+// FUSED (single pass, d = 64): the softmax warps also write dS^T into a
+// swizzled [128 keys][64 queries] shared-memory tile, the MMA warp adds
+// dQ(t) = dS K (M = 64 queries, both operands MN-major) into 64 more TMEM
+// columns, and the softmax warps add each partial into the fp32 dQ buffer
+// one step later (the dQ reduction across CTAs of wittx "FlashAttention-4",
+// 反向传播的优化), in key-tile order when a semaphore per query tile is given.
+template <int DQK, int DV, bool FUSED = false>
 struct DkdvCfg {
   static constexpr int QB = 64;                     // query rows per step
   // TMEM columns: S^T | dP^T | P^T,dS^T | dV | dK | [V] | [K]
@@ -94,8 +101,12 @@ struct DkdvCfg {
   static constexpr int OFF_V = K_BYTES;
   static constexpr int OFF_ST = OFF_V + V_BYTES;
   static constexpr int OFF_VEC = OFF_ST + NST * STAGE;  // per stage: [QB] -LSE*log2e, [QB] -D
-  static constexpr int OFF_BAR = OFF_VEC + NST * 2 * QB * 4;
+  static constexpr int OFF_DS = (OFF_VEC + NST * 2 * QB * 4 + 1023) / 1024 * 1024;  // FUSED: dS^T tile
+  static constexpr int OFF_BAR = FUSED ? OFF_DS + KB * QB * 2 : OFF_VEC + NST * 2 * QB * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  // FUSED: the 64 x DQK dQ partial (M = 64: row m in lane 32 (m / 16) + m % 16)
+  static constexpr uint32_t tdQ = tK + (K_TMEM ? DQK / 2 : 0);
+  static_assert(!FUSED || (DQK == 64 && DV == 64 && tdQ + DQK <= 512), "single pass: d = 64");
   static_assert(BASE <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -114,13 +125,32 @@ struct DkdvBars {
   uint32_t tmem_base;
 };
 
+// Waits until *sem >= target (acquire). Gives up like mbar_wait (10 s and
+// 2^22 polls, or at once when another wait already failed), recording
+// DEV_TIMEOUT_SEM at `where`.
+__device__ __forceinline__ bool sem_wait(const int* sem, int target, uint32_t* status, uint32_t where) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(sem) : "memory");
+    if (v >= target) return true;
+    if (i > 64) __nanosleep(128);
+    if ((i & 0xFFu) == 0xFFu) {
+      if (status && *reinterpret_cast<volatile uint32_t*>(status) != 0) return false;
+      if (i > kMinPolls && globaltimer_ns() - t0 > kWaitNs) break;
+    }
+  }
+  record_error(status, DEV_TIMEOUT_SEM, where);
+  return false;
+}
+
 // SPARSE: the key block's query tiles are those of the query blocks in its
 // transposed block-sparse list (a.q_index), not m_begin .. m_end - 1.
-template <int DQK, int DV, bool SPARSE = false, int MOD = 0>
+template <int DQK, int DV, bool SPARSE = false, int MOD = 0, bool FUSED = false>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo, const BwdArgs a) {
-  using C = DkdvCfg<DQK, DV>;
+  using C = DkdvCfg<DQK, DV, FUSED>;
   constexpr int QB = C::QB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -128,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sV = smem + C::OFF_V;
   uint8_t* sST = smem + C::OFF_ST;
   float* sVec = reinterpret_cast<float*>(smem + C::OFF_VEC);  // [NST][2][QB], beside the stages
+  uint8_t* sDS = smem + C::OFF_DS;                             // FUSED only
   DkdvBars* bar = reinterpret_cast<DkdvBars*>(smem + C::OFF_BAR);
 
   // (unit, head) is the slow index so that resident CTAs share a few heads'
@@ -318,6 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t da = tbase + C::tPdS + 32 * (kk / 2) + 16 + (kk % 2) * 8;
           mma_ts(tbase + C::tdK, da, desc_add(mq, kk * 2048), idK, kk > 0 ? 1u : acc0);
         }
+        if constexpr (FUSED) {  // dQ(t) = dS K over the tile's 128 keys, 16 keys (16 rows of both tiles) per k-step
+          constexpr uint32_t idQ = idesc_bf16_f32(QB, DQK, true, true);
+          const uint64_t dsa = smem_desc(smem_u32(sDS), KB * 128, 1024, SWZ_128B);
+          const uint64_t kmn = smem_desc(kb, KB * 128, 1024, SWZ_128B);  // K as the MN-major B operand
+#pragma unroll
+          for (int kk = 0; kk < KB / 16; ++kk)
+            mma_ss(tbase + C::tdQ, desc_add(dsa, kk * 2048), desc_add(kmn, kk * 2048), idQ, kk > 0 ? 1u : 0u);
+        }
         mma_commit(&bar->pds_free);
         mma_commit(&bar->st_empty[t % C::NST]);
       }
@@ -353,6 +392,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar->kv_tmem);
     const float2 sl2v = make_float2(sl2, sl2);
+    // FUSED: adds this warp's part of the dQ partial of the query tile at tq0 (lanes
+    // 0-15 hold rows 16 * quarter + lane, columns 32 * wg ...) into the fp32 buffer.
+    // With semaphores each warp first waits until every earlier key tile's eight
+    // warps have added this tile, and counts itself in afterwards.
+    auto reduce_dq = [&](const uint32_t (&qv)[32], int tq0) -> bool {
+      bool good = true;
+      int* sem = a.dq_sem ? a.dq_sem + (static_cast<int64_t>(U.unit) * a.heads + h) * a.n_qt64 + tq0 / QB : nullptr;
+      if (sem != nullptr) {
+        if (lane == 0) good = sem_wait(sem, n * (kSoftThreads / 32), a.status, 0x1320);
+        good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
+      }
+      const int m = 16 * static_cast<int>(quarter) + static_cast<int>(lane);
+      if (lane < 16 && tq0 + m < U.nq) {
+        float* dst = a.dq_acc + ((static_cast<int64_t>(U.b) * a.heads + h) * a.seqlen_q + U.q_start + tq0 + m) * DQK +
+                     32 * wg;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4 * c),
+                       "f"(__uint_as_float(qv[4 * c])), "f"(__uint_as_float(qv[4 * c + 1])),
+                       "f"(__uint_as_float(qv[4 * c + 2])), "f"(__uint_as_float(qv[4 * c + 3]))
+                       : "memory");
+      }
+      if (sem != nullptr) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(sem, 1);
+      }
+      return good;
+    };
     for (int t = 0; t < T && ok; ++t) {
       const int q0 = q_row(t);
       ok = mbar_wait_warp(&bar->s_full, static_cast<uint32_t>(t) & 1u, a.status, 0x1300);
@@ -409,22 +477,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the causal boundary and a key row past the end need the per-element test.
       if (key_ok && q0 + 32 * wg >= i_vis) row(false);
       else row(true);
-      if (t > 0) {  // dV(t-1), dK(t-1) must have read the previous P^T, dS^T
+      if (t > 0) {  // dV(t-1), dK(t-1) (and dQ(t-1)) must have read the previous P^T, dS^T
         ok = mbar_wait_warp(&bar->pds_free, static_cast<uint32_t>(t - 1) & 1u, a.status, 0x1305);
         if (!ok) break;
         tc_fence_after();
       }
+      uint32_t qv[32];  // FUSED: dQ(t-1), complete once pds_free(t-1) has
+      if constexpr (FUSED) {
+        if (t > 0) {
+          tmem_ld32(lane_base + C::tdQ + 32 * wg, qv);
+          tmem_wait_ld();
+        }
+      }
       tmem_st16(lane_base + my_pds, pw);
       tmem_st16(lane_base + my_pds + 16, dw);
+      if constexpr (FUSED) {  // key row j of dS^T: query columns 32 wg .. 32 wg + 31, 16-byte chunks swizzled by j
+        uint8_t* rowp = sDS + j * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4*>(rowp + (((4 * wg + u) ^ (j & 7)) << 4)) =
+              make_uint4(dw[4 * u], dw[4 * u + 1], dw[4 * u + 2], dw[4 * u + 3]);
+        fence_proxy_async_smem();
+      }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar->ds_full);
+      if constexpr (FUSED) {
+        if (t > 0) ok = reduce_dq(qv, q_row(t - 1)) && ok;
+      }
     }
     // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
     if (ok && T > 0) {
       ok = mbar_wait_warp(&bar->acc_full, 0, a.status, 0x1310);
       tc_fence_after();
+    }
+    if constexpr (FUSED) {  // the last step's dQ partial
+      if (ok && T > 0) {
+        uint32_t qv[32];
+        tmem_ld32(lane_base + C::tdQ + 32 * wg, qv);
+        tmem_wait_ld();
+        ok = reduce_dq(qv, q_row(T - 1));
+      }
     }
     const bool store = key_ok;
     if (wg == 0) {
@@ -1251,11 +1345,11 @@ cudaError_t set_smem(K kern, int bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int DQK, int DV, bool SPARSE, int MOD = 0>
+template <int DQK, int DV, bool SPARSE, int MOD = 0, bool FUSED = false>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                           const BwdArgs& a, cudaStream_t stream) {
-  using C = DkdvCfg<DQK, DV>;
-  auto kern = dkdv_kernel<DQK, DV, SPARSE, MOD>;
+  using C = DkdvCfg<DQK, DV, FUSED>;
+  auto kern = dkdv_kernel<DQK, DV, SPARSE, MOD, FUSED>;
   static PerDeviceOnce once;
   cudaError_t e = once.run([&] { return set_smem(kern, C::SMEM); });
   if (e != cudaSuccess) return e;

@@ -194,8 +194,21 @@ struct BwdArgs {
   // Block-sparse: 1 = lists per (batch, head): forward set (b * heads + h) at
   // count index (b * heads + h) * n_qb256, transposed set at (b * heads + h) * n_kb.
   int lists_per_head;
+  // Single-pass backward only (nullptr otherwise): fp32 dQ, [units][heads][seqlen_q][d]
+  // (zeroed), to which the dK/dV kernel adds its dQ partials; with dq_sem set,
+  // one semaphore per (unit, head, 64-row query tile), n_qt64 tiles per (unit,
+  // head), orders the adds by key tile.
+  float* dq_acc;
+  int* dq_sem;
+  int n_qt64;
 };
 
+// Single-pass backward (d_qk = d_v = 64): dK, dV and the fp32 dQ partials of
+// the dK/dV kernel (a.dq_acc, ordered by a.dq_sem when set), then
+// dQ = bf16(dq_acc * scale).
+cudaError_t launch_bwd_single_pass(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_dq_convert(const BwdArgs& a, int d, cudaStream_t stream);
 // D = rowsum(dO * O) into args.dsum.
 cudaError_t launch_bwd_preprocess(int d_v, const BwdArgs& a, cudaStream_t stream);
 // dK, dV (KV-stationary) and dQ (Q-stationary). Maps: q, k, v, dO. With

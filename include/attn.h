@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 3
+#define ATTN_ABI_VERSION 4
 
 typedef enum {
   ATTN_OK = 0,
@@ -211,6 +211,21 @@ typedef struct attn_bwd_params {
    * stream after the D = rowsum(dO * O) pass [0], after the dK/dV kernel [1]
    * and after the dQ kernel [2], for timing the phases. */
   void* phase_events[3];
+  /* single_pass != 0: the backward of wittx "FlashAttention-4", 反向传播的优化:
+   * one key-stationary kernel computes dK, dV and, per 64-query step, the dQ
+   * partial dS K, which it adds into an fp32 dQ buffer in the workspace
+   * (red.global.add in L2); a last pass writes dQ * softmax_scale in bf16.
+   * With deterministic != 0 the adds to each 64-row query tile are ordered
+   * by key tile through one int32 semaphore per (batch or sequence, head,
+   * tile): a key tile waits until every earlier one has added (bounded wait,
+   * else ATTN_ERR_TIMEOUT from attn_get_device_status), so repeated calls
+   * are bitwise identical; with deterministic == 0 the adds land in the
+   * hardware's order. Only d_qk = d_v = 64, bf16 inputs, dense or varlen,
+   * no block lists, no score modification, cta_pair == 0 (else
+   * ATTN_ERR_UNSUPPORTED). The workspace adds, each rounded up to 256,
+   * 4 x heads x query rows x 64 bytes for the fp32 dQ and, deterministic
+   * only, 4 x (batch or num_seqs) x heads x ceil(max query length / 64). */
+  int32_t single_pass;
 } attn_bwd_params;
 
 /* Bytes of device workspace the matching call needs (0 means none: pass NULL).

@@ -381,3 +381,27 @@ def test_e4m3_is_forward_only(lib, _abi):
     assert lib.attn_bwd(ctypes.byref(b), None, 0, None) == UNSUPPORTED
     b.fwd.input_dtype = 2
     assert lib.attn_bwd(ctypes.byref(b), None, 0, None) == INVALID
+
+
+def test_single_pass_workspace_and_rejections_without_a_gpu(lib, _abi):
+    r256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    p = _abi.AttnBwdParams()
+    p.fwd = _valid_fwd(_abi)  # B1 H4 N128 d64
+    p.dout = p.dq = p.dk = p.dv = 0x10000
+    for t in ("do", "dq", "dk", "dv"):
+        setattr(p, f"{t}_batch_stride", 128 * 4 * 64)
+        setattr(p, f"{t}_row_stride", 4 * 64)
+        setattr(p, f"{t}_head_stride", 64)
+    base = lib.attn_bwd_workspace_size(ctypes.byref(p))
+    p.single_pass = 1
+    assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == base + r256(4 * 128 * 64 * 4)  # the fp32 dQ
+    p.deterministic = 1  # plus one semaphore per (batch, head, 64-row tile)
+    assert lib.attn_bwd_workspace_size(ctypes.byref(p)) == base + r256(4 * 128 * 64 * 4) + r256(1 * 4 * 2 * 4)
+    p.cta_pair = 1
+    assert lib.attn_bwd(ctypes.byref(p), None, 0, None) == UNSUPPORTED
+    p.cta_pair = 0
+    p.fwd.score_mod, p.fwd.softcap = 1, 30.0
+    assert lib.attn_bwd(ctypes.byref(p), None, 0, None) == UNSUPPORTED
+    p.fwd.score_mod = 0
+    p.fwd.d_qk = p.fwd.d_v = 128
+    assert lib.attn_bwd(ctypes.byref(p), None, 0, None) == UNSUPPORTED
