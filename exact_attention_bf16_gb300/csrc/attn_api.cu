@@ -571,7 +571,9 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
     int64_t* scratch = reinterpret_cast<int64_t*>(lbase + (kv.use ? kv.list_bytes : 0) + (qp.use ? qp.list_bytes : 0));
     if (kv.use) {
       TileEntry* list = reinterpret_cast<TileEntry*>(lbase);
-      e = launch_tile_list(f.cu_seqlens_q, f.cu_seqlens_k, f.num_seqs, f.heads, 128, true, false, kv.max_nblk, list,
+      // the deterministic single pass launches key tiles in descending order (its adds' order)
+      const bool desc = p->single_pass && p->deterministic;
+      e = launch_tile_list(f.cu_seqlens_q, f.cu_seqlens_k, f.num_seqs, f.heads, 128, true, desc, kv.max_nblk, list,
                            scratch, kv.bound, stream);
       if (e != cudaSuccess) return cuda_fail(e, "bwd tile list");
       a.tiles_kv = list;

@@ -166,7 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // under the causal mask) come first.
   Unit U;
   int h, n;
-  if (!bwd_work(a, a.tiles_kv, a.n_kblk, false, U, h, n)) return;
+  // FUSED with semaphores: key tiles in descending order, the shortest (fewest
+  // query tiles under the causal mask) first, matching the adds' order below
+  if (!bwd_work(a, a.tiles_kv, a.n_kblk, FUSED && a.dq_sem != nullptr, U, h, n)) return;
   const int k0 = n * KB;
   if (k0 >= U.nk) return;
   int m_begin = 0;
@@ -394,13 +396,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float2 sl2v = make_float2(sl2, sl2);
     // FUSED: adds this warp's part of the dQ partial of the query tile at tq0 (lanes
     // 0-15 hold rows 16 * quarter + lane, columns 32 * wg ...) into the fp32 buffer.
-    // With semaphores each warp first waits until every earlier key tile's eight
-    // warps have added this tile, and counts itself in afterwards.
+    // With semaphores the adds to a query tile go from the highest contributing key
+    // tile down (SPT order: wittx "FlashAttention-4", 反向传播的优化): the key tiles
+    // that see query tile m are 0 .. n_m - 1 (a prefix, since m_begin grows with
+    // n), so each warp waits until the eight warps of each of the n_m - 1 - n tiles
+    // above it have added this tile, and counts itself in afterwards.
     auto reduce_dq = [&](const uint32_t (&qv)[32], int tq0) -> bool {
       bool good = true;
       int* sem = a.dq_sem ? a.dq_sem + (static_cast<int64_t>(U.unit) * a.heads + h) * a.n_qt64 + tq0 / QB : nullptr;
       if (sem != nullptr) {
-        if (lane == 0) good = sem_wait(sem, n * (kSoftThreads / 32), a.status, 0x1320);
+        int n_m = ceil_div(U.nk, KB);
+        if (a.causal) {  // key tiles with 128 n - (nk - nq) <= the tile's last row
+          const int lim = tq0 + QB - 1 + (U.nk - U.nq);
+          n_m = min(n_m, lim / KB + 1);  // lim >= 0: this tile sees key tile n
+        }
+        if (lane == 0) good = sem_wait(sem, (n_m - 1 - n) * (kSoftThreads / 32), a.status, 0x1320);
         good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
       }
       const int m = 16 * static_cast<int>(quarter) + static_cast<int>(lane);
