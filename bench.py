@@ -286,6 +286,15 @@ def measure_configs(ea, dev, stream) -> dict:
             r = dense(w, bwd=False, emu=emu)
             rec(f"dense_d128_B4_N8192_{'causal' if causal else 'noncausal'}_exp2_emu_1_in_{emu}", w, r["fwd"],
                 exp2_emu_period=emu)
+    for causal in (False, True):  # the two-SM (cta_group::2, M = 256 pair) forward on the headline shape
+        w = workloads.dense_d128(8192, causal)
+        t = workloads.make_dense(w, device=dev, with_do=False)
+        o, lse = ea.attn_fwd(t["q"], t["k"], t["v"], causal=causal, softmax_scale=w.scale, cta_pair=True)
+        f = time_ms(lambda: ea.attn_fwd(t["q"], t["k"], t["v"], causal=causal, softmax_scale=w.scale, out=o, lse=lse,
+                                        cta_pair=True), stream)
+        rec(f"dense_d128_B4_N8192_{'causal' if causal else 'noncausal'}_fwd_cta_pair", w, f, cta_pair=True)
+        del t, o, lse
+        torch.cuda.empty_cache()
     for causal in (False, True):  # the two-SM (cta_group::2) dK/dV kernel on the headline shape
         w = workloads.dense_d128(8192, causal)
         t = workloads.make_dense(w, device=dev)

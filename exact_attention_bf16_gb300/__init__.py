@@ -126,13 +126,13 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool 
              lse: Optional[torch.Tensor] = None, rescale_stats: Optional[torch.Tensor] = None,
              exp2_emu_period: int = 0, softcap: Optional[float] = None,
              alibi_slopes: Optional[torch.Tensor] = None, q_descale: float = 1.0, k_descale: float = 1.0,
-             v_descale: float = 1.0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+             v_descale: float = 1.0, cta_pair: bool = False, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Dense forward. q [B, Nq, H, d_qk], k [B, Nk, H, d_qk], v [B, Nk, H, d_v] (bf16, CUDA).
     Returns (O [B, Nq, H, d_v] bf16, LSE [B, H, Nq] fp32, natural log). ``exp2_emu_period`` (0, 4, 8)
     sends one column in that many of every row's exp2 to the FMA-pipe polynomial. ``softcap`` or
     ``alibi_slopes`` select a score modification (include/attn.h, attn_fwd_params.score_mod).
     q, k, v may instead all be torch.float8_e4m3fn (d = 128), standing for their values times
-    ``q_descale``, ``k_descale``, ``v_descale``."""
+    ``q_descale``, ``k_descale``, ``v_descale``. ``cta_pair`` runs the two-SM forward (d = 128)."""
     f8 = _check_inputs(q, k, v, 4)
     B, Nq, H, dqk = q.shape
     Nk, dv = k.shape[1], v.shape[-1]
@@ -153,6 +153,7 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool 
     p.exp2_emu_period = int(exp2_emu_period)
     _set_score_mod(p, q, softcap, alibi_slopes)
     _set_input_dtype(p, f8, q_descale, k_descale, v_descale)
+    p.cta_pair = 1 if cta_pair else 0
     ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_fwd(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_fwd")
     return out, lse
@@ -235,7 +236,8 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
                     lse: Optional[torch.Tensor] = None, rescale_stats: Optional[torch.Tensor] = None,
                     exp2_emu_period: int = 0, softcap: Optional[float] = None,
                     alibi_slopes: Optional[torch.Tensor] = None, q_descale: float = 1.0, k_descale: float = 1.0,
-                    v_descale: float = 1.0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                    v_descale: float = 1.0, cta_pair: bool = False,
+                    stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Packed variable-length forward. q [total_q, H, d_qk], k/v [total_k, H, d]; cu_seqlens int32 on
     the device. Returns (O [total_q, H, d_v], LSE [H, total_q]). Score modifications and E4M3 inputs
     as in :func:`attn_fwd`, positions counted within each sequence."""
@@ -261,6 +263,7 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlen
     p.exp2_emu_period = int(exp2_emu_period)
     _set_score_mod(p, q, softcap, alibi_slopes)
     _set_input_dtype(p, f8, q_descale, k_descale, v_descale)
+    p.cta_pair = 1 if cta_pair else 0
     ws, nbytes = _workspace(_lib.attn_fwd_workspace_size(ctypes.byref(p)), q.device)
     _abi.check(_lib.attn_fwd_varlen(ctypes.byref(p), _ptr(ws), nbytes, _stream(stream)), "attn_fwd_varlen")
     return out, lse

@@ -10,7 +10,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libattn_gb300.so")
 HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "attn.h")
 
-ABI_VERSION = 4
+ABI_VERSION = 5
 BWD_NOALLOC_SCRATCH_BYTES = 8 << 20  # ATTN_BWD_NOALLOC_SCRATCH_BYTES
 
 STATUS = {
@@ -44,7 +44,7 @@ class AttnFwdParams(ctypes.Structure):
         ("rescale_stats", c_vp),
         ("score_mod", c_i32), ("softcap", ctypes.c_float), ("alibi_slopes", c_vp),
         ("input_dtype", c_i32), ("q_descale", ctypes.c_float), ("k_descale", ctypes.c_float),
-        ("v_descale", ctypes.c_float),
+        ("v_descale", ctypes.c_float), ("cta_pair", c_i32),
     ]
 
 

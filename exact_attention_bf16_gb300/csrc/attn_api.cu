@@ -287,8 +287,8 @@ size_t fwd_v16_bytes(const attn_fwd_params* p, bool varlen) {
   if (rows <= 0) return 0;
   return static_cast<size_t>((rows * p->heads * p->d_v * 2 + 255) / 256 * 256);
 }
-ListPlan fwd_list_plan(const attn_fwd_params* p, bool varlen) {
-  return varlen ? list_plan(p->total_q, p->num_seqs, p->heads, p->max_seqlen_q, 256) : ListPlan{};
+ListPlan fwd_list_plan(const attn_fwd_params* p, bool varlen) {  // the pair forward takes no list
+  return varlen && !p->cta_pair ? list_plan(p->total_q, p->num_seqs, p->heads, p->max_seqlen_q, 256) : ListPlan{};
 }
 size_t fwd_workspace_bytes(const attn_fwd_params* p, bool varlen) {
   const size_t v16 = fwd_v16_bytes(p, varlen);
@@ -319,6 +319,9 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
   } else if (p->input_dtype != ATTN_INPUT_BF16) {
     return ATTN_ERR_INVALID_ARG;
   }
+  if (p->cta_pair && (p->d_qk != 128 || p->d_v != 128 || f8 || p->exp2_emu_period != 0 ||
+                      p->score_mod != ATTN_SCORE_NONE || sp.kv_count != nullptr || diag_limit))
+    return ATTN_ERR_UNSUPPORTED;
   const int nq_rows = varlen ? p->total_q : p->seqlen_q;
   const int nk_rows = varlen ? p->total_k : p->seqlen_k;
   const int units = varlen ? p->num_seqs : p->batch;
@@ -349,7 +352,7 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
   a.cu_q = varlen ? p->cu_seqlens_q : nullptr;
   a.cu_k = varlen ? p->cu_seqlens_k : nullptr;
   a.num_units = units;
-  a.n_mblk = (max_q + 255) / 256;
+  a.n_mblk = p->cta_pair ? (max_q + 511) / 512 : (max_q + 255) / 256;  // 512-row blocks per CTA pair
   a.scale_log2 = p->softmax_scale * 1.4426950408889634f;
   if (f8) {  // S of the codes times both descales
     a.scale_log2 = p->softmax_scale * p->q_descale * p->k_descale * 1.4426950408889634f;
@@ -420,9 +423,18 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
     a.tiles = list;
     a.n_tiles = lp.bound;
   }
-  if (f8) e = launch_fwd_e4m3(tq, tk, tv16, a, stream);
-  else if (sp.kv_count) e = launch_fwd_sparse(p->d_qk, p->d_v, tq, tk, tv, tv16, a, stream);
-  else e = launch_fwd(p->d_qk, p->d_v, tq, tk, tv, tv16, a, stream);
+  if (p->cta_pair) {
+    CUtensorMap tk_h;  // 64-key boxes: each CTA of a pair loads half of every K tile
+    ATTN_TRY(make_map(&tk_h, p->k, p->d_qk, p->heads, nk_rows, nb, p->k_batch_stride, p->k_row_stride,
+                      p->k_head_stride, 64));
+    e = launch_fwd_pair(tq, tk_h, tv, tv16, a, stream);
+  } else if (f8) {
+    e = launch_fwd_e4m3(tq, tk, tv16, a, stream);
+  } else if (sp.kv_count) {
+    e = launch_fwd_sparse(p->d_qk, p->d_v, tq, tk, tv, tv16, a, stream);
+  } else {
+    e = launch_fwd(p->d_qk, p->d_v, tq, tk, tv, tv16, a, stream);
+  }
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "fwd launch");
 }
 

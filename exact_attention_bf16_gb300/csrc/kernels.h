@@ -115,6 +115,10 @@ struct FwdArgs {
 
 cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tv16, const FwdArgs& a, cudaStream_t stream);
+// The forward over CTA pairs (d_qk = d_v = 128, bf16, dense or varlen without a
+// tile list): a.n_mblk counts 512-row blocks; tk_h has 64-row boxes.
+cudaError_t launch_fwd_pair(const CUtensorMap& tq, const CUtensorMap& tk_h, const CUtensorMap& tv,
+                            const CUtensorMap& tv16, const FwdArgs& a, cudaStream_t stream);
 // The forward with E4M3 Q, K, V (d_qk = d_v = 128, dense or tile list).
 cudaError_t launch_fwd_e4m3(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv16, const FwdArgs& a,
                             cudaStream_t stream);

@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 4
+#define ATTN_ABI_VERSION 5
 
 typedef enum {
   ATTN_OK = 0,
@@ -175,6 +175,16 @@ typedef struct attn_fwd_params {
   float q_descale;
   float k_descale;
   float v_descale;
+  /* Forward only (the backward's own cta_pair field selects its kernel):
+   * cta_pair != 0 runs the forward over clusters of two CTAs, the two-SM MMA
+   * (M = 256 pair) of wittx "FlashAttention-4", sections 反向传播的优化 and
+   * Blackwell的跛脚问题: each CTA holds 128 rows of a 256-row query tile and
+   * loads half of every K and V tile. Same results within rounding. Only
+   * d_qk = d_v = 128, bf16 inputs, exp2_emu_period 0, no score modification,
+   * dense or varlen, not block-sparse (else ATTN_ERR_UNSUPPORTED); varlen
+   * then launches from the block index (no tile list). The default (0) is
+   * the one-SM kernel, the faster of the two on GB300. */
+  int32_t cta_pair;
 } attn_fwd_params;
 
 /* Backward parameters. `fwd` holds q, k, v, the forward's outputs o and lse

@@ -405,3 +405,31 @@ def test_single_pass_workspace_and_rejections_without_a_gpu(lib, _abi):
     p.fwd.score_mod = 0
     p.fwd.d_qk = p.fwd.d_v = 128
     assert lib.attn_bwd(ctypes.byref(p), None, 0, None) == UNSUPPORTED
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda p: (setattr(p, "d_qk", 64), setattr(p, "d_v", 64)), UNSUPPORTED),  # d = 128 only
+    (lambda p: setattr(p, "exp2_emu_period", 4), UNSUPPORTED),
+    (lambda p: (setattr(p, "score_mod", 2), setattr(p, "alibi_slopes", 0x10000)), UNSUPPORTED),
+    (lambda p: (setattr(p, "input_dtype", 1), setattr(p, "q_descale", 1.0), setattr(p, "k_descale", 1.0),
+                setattr(p, "v_descale", 1.0)), UNSUPPORTED),
+])
+def test_pair_forward_rejects_without_a_gpu(lib, _abi, mutate, expect):
+    p = _valid_fwd(_abi)
+    p.d_qk = p.d_v = 128
+    for t in "qkvo":
+        setattr(p, f"{t}_batch_stride", 128 * 4 * 128)
+        setattr(p, f"{t}_row_stride", 4 * 128)
+        setattr(p, f"{t}_head_stride", 128)
+    p.cta_pair = 1
+    mutate(p)
+    assert lib.attn_fwd(ctypes.byref(p), None, 0, None) == expect
+
+
+def test_pair_forward_takes_no_tile_list(lib, _abi):
+    p = _valid_fwd(_abi)
+    p.cu_seqlens_q = p.cu_seqlens_k = 0x10000
+    p.num_seqs, p.total_q, p.total_k, p.max_seqlen_q, p.max_seqlen_k = 2, 300, 301, 200, 200
+    with_list = lib.attn_fwd_workspace_size(ctypes.byref(p))
+    p.cta_pair = 1
+    assert lib.attn_fwd_workspace_size(ctypes.byref(p)) == 256 + (301 * 4 * 64 * 2 + 255) // 256 * 256 < with_list
