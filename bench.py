@@ -42,19 +42,33 @@ WORKLOAD = dict(batch=4, heads=16, seqlen=8192, d_qk=128, d_v=128)
 
 # DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), scaled to the benchmark's launch, valid only for the
-# kernel source it was measured on (sha256 prefix of its .cu); null otherwise.
+# kernel sources it was measured on (sha256 prefix over the files the kernel
+# compiles from, KERNEL_SOURCES); null otherwise.
 # Measured on the non-causal B=2, H=16, N=8192 case (`bench.py --case`) and
 # scaled x2 to the benchmark's B=4 launch (traffic grows with the (batch, head) units).
+KERNEL_SOURCES = {
+    "dkdv_wide_kernel": ("bwd_kernels.cuh", "bwd_common.cuh", "ptx_sm100.cuh", "score_mod.cuh", "kernels.h"),
+    "dq_kernel": ("bwd_kernels.cuh", "bwd_common.cuh", "ptx_sm100.cuh", "score_mod.cuh", "kernels.h"),
+    "attn_fwd_kernel": ("fwd_kernel.cuh", "exp2_emu.cuh", "exp2_poly_coeffs.h", "ptx_sm100.cuh", "score_mod.cuh",
+                        "kernels.h"),
+}
 KERNEL_TRAFFIC_NCU = {
-    "dkdv_wide_kernel": {"source_sha": "e77285092c7bbf99", "bytes_per_launch": 2 * (270.671104e6 + 104.739584e6)},
-    "dq_kernel": {"source_sha": "e77285092c7bbf99", "bytes_per_launch": 2 * (270.743296e6 + 49.364736e6)},
-    "attn_fwd_kernel": {"source_sha": "7b89da9206a28ab1", "bytes_per_launch": 2 * (201.413632e6 + 45.540608e6)},
+    "dkdv_wide_kernel": {"source_sha": "2a0b25b19d556959", "bytes_per_launch": 2 * (270.682624e6 + 104.196864e6)},
+    "dq_kernel": {"source_sha": "2a0b25b19d556959", "bytes_per_launch": 2 * (270.701312e6 + 49.304320e6)},
+    "attn_fwd_kernel": {"source_sha": "f9d2be548df89172", "bytes_per_launch": 2 * (201.445376e6 + 45.798912e6)},
 }
 
 
-def sha_of(path: str) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def sha_of(*paths: str) -> str:
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_sources_sha(kernel: str) -> str:
+    return sha_of(*(os.path.join(ROOT, "exact_attention_bf16_gb300", "csrc", f) for f in KERNEL_SOURCES[kernel]))
 
 
 def dist_env():
@@ -562,8 +576,7 @@ def run_gpu(args):
     # The timed region lasts well under a second at full clock, so the burst
     # figure (a cuBLAS bf16 GEMM timed alone) is the matching denominator.
     peak = peaks.get("bf16_tflops", peaks.get("bf16_tflops_sustained"))
-    src = {"attn_fwd_kernel": "attn_fwd.cu"}.get(dom, "attn_bwd.cu")
-    src_sha = sha_of(os.path.join(ROOT, "exact_attention_bf16_gb300", "csrc", src))
+    src_sha = kernel_sources_sha(dom) if dom in KERNEL_SOURCES else None
     rec = KERNEL_TRAFFIC_NCU.get(dom, {})
     traffic = rec.get("bytes_per_launch") if rec.get("source_sha") == src_sha else None
     step_ms = sum(totals.values()) / args.steps
