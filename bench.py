@@ -43,7 +43,8 @@ WORKLOAD = dict(batch=4, heads=16, seqlen=8192, d_qk=128, d_v=128)
 # DRAM traffic per launch from one ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), scaled to the benchmark's launch, valid only for the
 # kernel sources it was measured on (sha256 prefix over the files the kernel
-# compiles from, KERNEL_SOURCES); null otherwise.
+# compiles from, KERNEL_SOURCES, with comments and blank lines removed, so that
+# documentation edits keep the figures); null otherwise.
 # Measured on the non-causal B=2, H=16, N=8192 case (`bench.py --case`) and
 # scaled x2 to the benchmark's B=4 launch (traffic grows with the (batch, head) units).
 KERNEL_SOURCES = {
@@ -53,17 +54,40 @@ KERNEL_SOURCES = {
                         "kernels.h"),
 }
 KERNEL_TRAFFIC_NCU = {
-    "dkdv_wide_kernel": {"source_sha": "2a0b25b19d556959", "bytes_per_launch": 2 * (270.682624e6 + 104.196864e6)},
-    "dq_kernel": {"source_sha": "2a0b25b19d556959", "bytes_per_launch": 2 * (270.701312e6 + 49.304320e6)},
-    "attn_fwd_kernel": {"source_sha": "f9d2be548df89172", "bytes_per_launch": 2 * (201.445376e6 + 45.798912e6)},
+    "dkdv_wide_kernel": {"source_sha": "48ca46f60a936855", "bytes_per_launch": 2 * (270.682624e6 + 104.196864e6)},
+    "dq_kernel": {"source_sha": "48ca46f60a936855", "bytes_per_launch": 2 * (270.701312e6 + 49.304320e6)},
+    "attn_fwd_kernel": {"source_sha": "604613b70be8c81b", "bytes_per_launch": 2 * (201.445376e6 + 45.798912e6)},
 }
+
+
+def code_only(text: str) -> str:
+    """C/C++ source without comments or blank lines (string literals kept)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':  # a string literal: copy through its closing quote
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).splitlines() if line.strip())
 
 
 def sha_of(*paths: str) -> str:
     h = hashlib.sha256()
     for path in paths:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,7 +1,8 @@
 // C-ABI entry points of libattn_gb300.so (declared in include/attn.h):
 // argument validation, TMA tensor-map encoding, workspace accounting and
-// kernel launches. All compute runs in the kernels of attn_fwd.cu and
-// attn_bwd.cu; this file holds host logic only.
+// kernel launches. All compute runs in the CUDA kernels (fwd_kernel.cuh and
+// bwd_kernels.cuh with the translation units that instantiate them, the pair
+// kernels, schedule.cu); this file holds host logic only.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>

@@ -1,4 +1,4 @@
-// Pieces shared by the backward kernels (attn_bwd.cu, attn_bwd_pair.cu):
+// Pieces shared by the backward kernels (bwd_kernels.cuh, attn_bwd_pair.cu):
 // tile sizes, warp roles, row stores and the bounds of a work unit.
 #pragma once
 #include <cuda_bf16.h>

@@ -27,7 +27,7 @@
 //
 // This header holds the dK/dV and dQ kernel templates and their launch
 // templates; attn_bwd.cu instantiates them without a score modification,
-// attn_bwd_mod.cu with one.
+// attn_bwd_mod.cu with one, attn_bwd_fused.cu the single-pass d = 64 kernel.
 #pragma once
 #include <cuda_bf16.h>
 

@@ -31,7 +31,8 @@
 //
 // This header holds the kernel template and its launch template; the
 // translation units that instantiate it are attn_fwd.cu (no score
-// modification) and attn_fwd_mod.cu (the score-modification variants).
+// modification), attn_fwd_mod.cu (the score-modification variants) and
+// attn_fwd_fp8.cu (E4M3 inputs). The two-SM forward is attn_fwd_pair.cu.
 #pragma once
 #include <cuda_bf16.h>
 
