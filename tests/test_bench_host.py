@@ -103,3 +103,17 @@ def test_causal_pair_count_matches_brute_force():
         brute = sum(min(max(i + nk - nq + 1, 0), nk) for i in range(nq))
         assert workloads.causal_pairs(nq, nk) == brute
     assert workloads.causal_pairs(8192, 8192) == 8192 * 8192 / 2  # the half-square convention
+
+
+def test_traffic_key_ignores_comments_only():
+    """The roofline's traffic figures stay valid across documentation edits of the
+    kernel sources, and go null on any code change."""
+    import bench
+    a = 'int x = 1; // one\n/* block\n comment */\nconst char* s = "a // b";\n\n  y = x;  \n'
+    b = 'int x = 1;\nconst char* s = "a // b";\n  y = x;\n// trailing\n'
+    c = 'int x = 2;\nconst char* s = "a // b";\n  y = x;\n'
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(c)
+    assert '"a // b"' in bench.code_only(a)
+    for k in bench.KERNEL_SOURCES:
+        assert len(bench.kernel_sources_sha(k)) == 16
