@@ -656,15 +656,23 @@ def run_case(args):
     import workloads
     w = workloads.Workload("case", 2, 16, 8192, 8192, args.dqk, min(args.dqk, 128), args.causal, seed=0)
     t = workloads.make_dense(w, device="cuda")
+    q, k, v, kw = t["q"], t["k"], t["v"], {}
+    if args.e4m3:  # the E4M3 forward: codes of x / descale, descale = max|x| / 448
+        for n in ("q", "k", "v"):
+            kw[f"{n}_descale"] = float(t[n].abs().max()) / 448.0
+        q, k, v = ((t[n].float() / kw[f"{n}_descale"]).to(torch.float8_e4m3fn) for n in ("q", "k", "v"))
     o, lse = ea.attn_fwd(t["q"], t["k"], t["v"], causal=w.causal)
     for _ in range(4):
         if args.case == "fwd":
-            ea.attn_fwd(t["q"], t["k"], t["v"], causal=w.causal, out=o, lse=lse, exp2_emu_period=args.emu)
+            ea.attn_fwd(q, k, v, causal=w.causal, out=o, lse=lse, exp2_emu_period=args.emu, cta_pair=args.cta_pair,
+                        **kw)
         else:
-            ea.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=w.causal, cta_pair=args.cta_pair)
+            ea.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], causal=w.causal, cta_pair=args.cta_pair,
+                        single_pass=args.single_pass)
     torch.cuda.synchronize()
     ea.attn_get_device_status()
-    print(f"case {args.case} d_qk={args.dqk} causal={int(args.causal)} emu={args.emu} pair={int(args.cta_pair)} done")
+    print(f"case {args.case} d_qk={args.dqk} causal={int(args.causal)} emu={args.emu} pair={int(args.cta_pair)} "
+          f"e4m3={int(args.e4m3)} single_pass={int(args.single_pass)} done")
     return 0
 
 
@@ -674,7 +682,9 @@ def main(argv=None):
     ap.add_argument("--causal", action="store_true", help="causal mask for --case")
     ap.add_argument("--dqk", type=int, default=128, choices=[64, 128, 192], help="head dim of Q/K for --case")
     ap.add_argument("--emu", type=int, default=0, choices=[0, 4, 8], help="exp2 emulation period for --case fwd")
-    ap.add_argument("--cta-pair", action="store_true", help="two-SM dK/dV kernel for --case bwd")
+    ap.add_argument("--cta-pair", action="store_true", help="two-SM kernel for --case fwd / bwd (d = 128)")
+    ap.add_argument("--e4m3", action="store_true", help="E4M3 inputs for --case fwd (d = 128)")
+    ap.add_argument("--single-pass", action="store_true", help="single-pass backward for --case bwd (d = 64)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
