@@ -368,6 +368,10 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
   a.max_kv = sp.max_kv;
   a.lists_per_head = sp.lists_per_head;
   a.spin_limit = diag_limit;
+  a.n_groups = units * p->heads;
+  if (p->causal && sp.kv_count == nullptr && a.n_mblk >= 8)  // heavy blocks first across a group of heads
+    a.n_groups = group_count(units * p->heads, static_cast<int64_t>(varlen ? p->max_seqlen_k : p->seqlen_k) *
+                                                   (p->d_qk * (f8 ? 1 : 2) + p->d_v * 2));
   fill_score_mod(a, p);
   cudaError_t e = status_ptr(&a.status);
   if (e != cudaSuccess) return cuda_fail(e, "status word");
@@ -562,6 +566,11 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
   a.scale = f.softmax_scale;
   a.scale_log2 = f.softmax_scale * 1.4426950408889634f;
   a.causal = f.causal ? 1 : 0;
+  a.n_groups = a.num_units * f.heads;
+  // heavy blocks first across a group of heads (the deterministic single pass keeps its add order)
+  if (f.causal && sp.kv_count == nullptr && !(p->single_pass && p->deterministic) && a.n_kblk >= 16)
+    a.n_groups = group_count(a.num_units * f.heads,
+                             static_cast<int64_t>(max_q > max_k ? max_q : max_k) * (f.d_qk + f.d_v) * 2);
   fill_score_mod(a, &f);
   const int n_kb_sparse = (f.seqlen_k + 127) / 128;
   if (sp.kv_count) {

@@ -55,9 +55,9 @@ __device__ __forceinline__ bool bwd_work(const BwdArgs& a, const TileEntry* tile
     blk = t1.y;
     return true;
   }
-  const int bh = static_cast<int>(blockIdx.x) / nblk;
-  const int r = static_cast<int>(blockIdx.x) % nblk;
-  blk = descending ? nblk - 1 - r : r;
+  const GridSlot g = grid_slot(static_cast<int>(blockIdx.x), a.num_units * a.heads, nblk, a.n_groups);
+  const int bh = g.pair;
+  blk = descending ? nblk - 1 - g.rank : g.rank;
   h = bh % a.heads;
   U = unit_bounds(a, bh / a.heads);
   return true;

@@ -151,8 +151,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (t1.z < 0) return;  // an empty entry past the real ones
     q_start = t0.x, nq = t0.y, k_start = t0.z, nk = t0.w, h = t1.x, mblk = t1.y, b = 0;
   } else {
-    const int bh = static_cast<int>(blockIdx.x) / a.n_mblk;
-    mblk = a.n_mblk - 1 - static_cast<int>(blockIdx.x) % a.n_mblk;
+    const GridSlot g = grid_slot(static_cast<int>(blockIdx.x), a.num_units * a.heads, a.n_mblk, a.n_groups);
+    const int bh = g.pair;
+    mblk = a.n_mblk - 1 - g.rank;
     const int unit = bh / a.heads;
     h = bh % a.heads;
     b = unit;
@@ -204,6 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkv_max = max(nkv[0], nkv[1]);
   const PollLimit poll_lim = DIAG ? PollLimit{a.spin_limit} : kNoPollLimit;  // of the waits below
 
+  // Early copies by thread 0 for dense d_qk <= 128 without a score
+  // modification. Otherwise (d_qk = 192: measured faster; block-sparse and
+  // score modifications: fewer spills) the producer copies Q first, then the
+  // K/V ring, after the block barrier.
+  constexpr bool kEarlyQ = DQK <= 128 && !SPARSE && MOD == kModNone, kEarlyK = kEarlyQ;
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     for (int i = 0; i < QT; ++i) {
@@ -218,6 +224,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bar->mma_done, 1);
     fence_barrier_init();
+    if (!DIAG && kEarlyQ) {
+      // Q (and, dense, K of the first step right behind Q tile 0: all the first S
+      // needs) copied before the TMEM allocation and the block barrier
+      tma_prefetch_desc(&tmq);
+      for (int i = 0; i < QT; ++i) {
+        mbar_arrive_expect_tx(&bar->q_full[i], C::Q_BYTES);
+        for (int c = 0; c < C::QCH; ++c)
+          tma_load_4d(sQ + i * C::Q_BYTES + c * kChunk, &tmq, &bar->q_full[i], c * C::QX, h, q_start + row0 + i * BM, b);
+        if (kEarlyK && i == 0 && nkv_max > 0) {
+          const int kb0 = key_block(0);
+          mbar_arrive_expect_tx(&bar->kv_full[0], C::K_BYTES);
+          for (int c = 0; c < C::QCH; ++c)
+            tma_load_4d(sKV + c * kChunk, &tmk, &bar->kv_full[0], c * C::QX, h, k_start + kb0 * BN, b);
+        }
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(&bar->tmem_base, 512);
@@ -233,21 +255,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ======================= TMA producer ===================================
     if (lane == 0 && !DIAG) {
-      tma_prefetch_desc(&tmq);
-      tma_prefetch_desc(&tmk);
-      for (int i = 0; i < QT; ++i) {
-        mbar_arrive_expect_tx(&bar->q_full[i], C::Q_BYTES);
-        for (int c = 0; c < C::QCH; ++c)
-          tma_load_4d(sQ + i * C::Q_BYTES + c * kChunk, &tmq, &bar->q_full[i], c * C::QX, h, q_start + row0 + i * BM, b);
+      if constexpr (!kEarlyQ) {
+        tma_prefetch_desc(&tmq);
+        for (int i = 0; i < QT; ++i) {
+          mbar_arrive_expect_tx(&bar->q_full[i], C::Q_BYTES);
+          for (int c = 0; c < C::QCH; ++c)
+            tma_load_4d(sQ + i * C::Q_BYTES + c * kChunk, &tmq, &bar->q_full[i], c * C::QX, h, q_start + row0 + i * BM, b);
+        }
       }
+      tma_prefetch_desc(&tmk);
       // read while the Q copies fly: V from the fp16 copy, or the bf16 original
       const CUtensorMap* tmvv = v_is_f16(a) ? &tmv16 : &tmv;
       tma_prefetch_desc(tmvv);
-      int issued = 0;
+      int issued = (kEarlyK && nkv_max > 0) ? 1 : 0;
       bool ok = true;
       for (int j = 0; j < nkv_max && ok; ++j) {
         const int kb = key_block(j);
-        for (int which = 0; which < 2 && ok; ++which) {
+        for (int which = (kEarlyK && j == 0) ? 1 : 0; which < 2 && ok; ++which) {  // K0 may be copied already
           const int u = 2 * j + which;
           const int slot = u % C::NSLOT;
           const uint32_t use = static_cast<uint32_t>(u / C::NSLOT);
@@ -279,8 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, false, false);
       const uint32_t idO = v_is_f16(a) ? idesc_f16_f32(BM, DV, false, true) : idesc_bf16_f32(BM, DV, false, true);
-      bool ok = mbar_wait(&bar->q_full[0], 0, a.status, 0x200, poll_lim) &&
-                mbar_wait(&bar->q_full[1], 0, a.status, 0x201, poll_lim);
+      // Q tile 0 first (copied before K0), tile 1 only before its first S
+      bool ok = mbar_wait(&bar->q_full[0], 0, a.status, 0x200, poll_lim);
       for (int j = 0; j <= nkv_max && ok; ++j) {
         const bool haveK = j < nkv_max;
         const bool haveV = j > 0;
@@ -310,6 +334,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j == nkv[i]) mma_commit(&bar->o_full[i]);
           }
           if (j < nkv[i]) {
+            if (j == 0 && i > 0) {
+              ok = mbar_wait(&bar->q_full[i], 0, a.status, 0x200u + i, poll_lim);
+              if (!ok) break;
+              tc_fence_after();
+            }
             // S_i = Q_i K_j^T, both K-major, 16-wide k-steps walking the 128-byte swizzle atoms
             const uint64_t dq = smem_desc(smem_u32(sQ + i * C::Q_BYTES), 16, 1024, SWZ_128B);
 #pragma unroll

@@ -59,6 +59,45 @@ struct TileEntry {
 static_assert(sizeof(TileEntry) == 32, "two 16-byte loads per CTA");
 constexpr int kMaxListBlocks = 2047;  // longest sequence, in blocks, a list is built for
 
+// Dispatch order of the dense launches (one CTA per (unit, head) pair and
+// block; the hardware starts CTAs roughly in index order as SMs free up). The
+// pairs are cut into n_groups groups of consecutive pairs (sizes differing by
+// at most one); a group's CTAs come before the next group's, and inside a group
+// the block rank is walked outermost, so the first-ranked blocks of all of the
+// group's pairs start before any later-ranked one. n_groups = n_pairs
+// gives one pair's blocks after another. With causal masking, and the kernels
+// ranking their blocks heaviest first, this keeps a heavy block from being
+// started last and running alone; the group is kept small enough for its K and V to stay in
+// L2 (group_count below). Bijective from [0, n_pairs * n_blk).
+struct GridSlot {
+  int pair, rank;
+};
+__host__ __device__ inline GridSlot grid_slot(int x, int n_pairs, int n_blk, int n_groups) {
+  if (n_groups < 1 || n_groups > n_pairs) n_groups = n_pairs;  // (unit, head)-major
+  const int base = n_pairs / n_groups, extra = n_pairs - base * n_groups;
+  const int big = (base + 1) * n_blk * extra;  // CTAs of the groups with base + 1 pairs
+  int size, start, r;
+  if (x < big) {
+    const int g = x / ((base + 1) * n_blk);
+    size = base + 1, start = g * (base + 1), r = x - g * (base + 1) * n_blk;
+  } else {
+    const int g = (x - big) / (base * n_blk);
+    size = base, start = extra * (base + 1) + g * base, r = x - big - g * base * n_blk;
+  }
+  const int rank = r / size;
+  return GridSlot{start + (r - rank * size), rank};
+}
+// Number of groups for n_pairs pairs that each stream bytes_per_pair of K and V
+// (or Q and dO) from L2: groups of at most 32 MB, about a quarter of GB300's L2.
+inline int group_count(int n_pairs, int64_t bytes_per_pair) {
+  constexpr int64_t kBudget = int64_t(32) << 20;
+  if (n_pairs <= 1) return 1;
+  int64_t g = bytes_per_pair > 0 ? kBudget / bytes_per_pair : n_pairs;
+  if (g < 1) g = 1;
+  if (g > n_pairs) g = n_pairs;
+  return static_cast<int>((n_pairs + g - 1) / g);
+}
+
 // Builds the list for num_seqs sequences (cu_q / cu_k offsets on the device):
 // sequences with the most blocks first (by key blocks when by_keys), then
 // head by head, blocks of a head in descending or ascending order. Writes
@@ -111,6 +150,9 @@ struct FwdArgs {
   // multiplied by v_descale (Q's and K's descales are in scale_log2).
   int input_e4m3;
   float v_descale;
+  // Dense launches (no tile list): dispatch groups of grid_slot; heads * num_units
+  // gives the (unit, head)-major order.
+  int n_groups;
 };
 
 cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -205,6 +247,9 @@ struct BwdArgs {
   float* dq_acc;
   int* dq_sem;
   int n_qt64;
+  // Dense launches (no tile list): dispatch groups of grid_slot, for the dK/dV
+  // and the dQ kernels; heads * num_units gives the (unit, head)-major order.
+  int n_groups;
 };
 
 // Single-pass backward (d_qk = d_v = 64): dK, dV and the fp32 dQ partials of
