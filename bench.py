@@ -54,9 +54,9 @@ KERNEL_SOURCES = {
                         "kernels.h"),
 }
 KERNEL_TRAFFIC_NCU = {
-    "dkdv_wide_kernel": {"source_sha": "48ca46f60a936855", "bytes_per_launch": 2 * (270.682624e6 + 104.196864e6)},
-    "dq_kernel": {"source_sha": "48ca46f60a936855", "bytes_per_launch": 2 * (270.701312e6 + 49.304320e6)},
-    "attn_fwd_kernel": {"source_sha": "604613b70be8c81b", "bytes_per_launch": 2 * (201.445376e6 + 45.798912e6)},
+    "dkdv_wide_kernel": {"source_sha": "c3d764140057f330", "bytes_per_launch": 2 * (270.651904e6 + 104.766720e6)},
+    "dq_kernel": {"source_sha": "c3d764140057f330", "bytes_per_launch": 2 * (270.819584e6 + 49.456128e6)},
+    "attn_fwd_kernel": {"source_sha": "36f499cf1b9474f7", "bytes_per_launch": 2 * (201.476608e6 + 46.993664e6)},
 }
 
 
