@@ -87,8 +87,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed. Returns false
-// (and records DEV_TIMEOUT_MBAR) if it does not within `limit` polls.
-// Waits until the phase with the given parity has completed. Returns false
 // (and records DEV_TIMEOUT_MBAR at `where`) after kWaitNs, or after `limit`
 // polls when a smaller limit is given.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status, uint32_t where,
