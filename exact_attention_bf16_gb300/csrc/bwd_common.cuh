@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "ptx_sm100.cuh"
 
 namespace gb300 {
 namespace bwd {
@@ -16,11 +17,7 @@ constexpr int kSoftThreads = 256;
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&w)[16]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int t = 0; t < 4; ++t) d[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
-}
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&w)[16]) { store_row64(dst, w); }
 
 // Sequence bounds of a work unit (dense: unit = batch index; varlen: b = 0 and
 // unit = the sequence).

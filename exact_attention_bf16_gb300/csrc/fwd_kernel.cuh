@@ -503,11 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float v1 = nkv[i] > 0 ? __uint_as_float(o[2 * t + 1]) * inv_l : 0.f;
         w[t] = pack_bf16x2(v0, v1);
       }
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) dst[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
-      }
+      if (store) store_row64(orow + c * 32, w);
     }
     if (store) {
       const float lse = (l > 0.f) ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;

@@ -441,6 +441,24 @@ __device__ __forceinline__ void regs_inc() {
 // ---------------------------------------------------------------------------
 // Small numeric helpers
 // ---------------------------------------------------------------------------
+// Stores 32 consecutive bf16 values (16 packed words, 64 bytes) of an output
+// row: two 32-byte stores when dst is 32-byte aligned (every sector written
+// whole by one instruction), else four 16-byte ones.
+__device__ __forceinline__ void store_row64(void* dst, const uint32_t (&w)[16]) {
+  if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(static_cast<uint8_t*>(dst) + 32 * t),
+                   "r"(w[8 * t]), "r"(w[8 * t + 1]), "r"(w[8 * t + 2]), "r"(w[8 * t + 3]), "r"(w[8 * t + 4]),
+                   "r"(w[8 * t + 5]), "r"(w[8 * t + 6]), "r"(w[8 * t + 7])
+                   : "memory");
+  } else {
+    uint4* d = static_cast<uint4*>(dst);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) d[t] = make_uint4(w[4 * t], w[4 * t + 1], w[4 * t + 2], w[4 * t + 3]);
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
