@@ -54,9 +54,9 @@ KERNEL_SOURCES = {
                         "kernels.h"),
 }
 KERNEL_TRAFFIC_NCU = {
-    "dkdv_wide_kernel": {"source_sha": "c3d764140057f330", "bytes_per_launch": 2 * (270.651904e6 + 104.766720e6)},
-    "dq_kernel": {"source_sha": "c3d764140057f330", "bytes_per_launch": 2 * (270.819584e6 + 49.456128e6)},
-    "attn_fwd_kernel": {"source_sha": "36f499cf1b9474f7", "bytes_per_launch": 2 * (201.476608e6 + 46.993664e6)},
+    "dkdv_wide_kernel": {"source_sha": "cf06f7aeb0bb5b1c", "bytes_per_launch": 2 * (270.809344e6 + 107.681024e6)},
+    "dq_kernel": {"source_sha": "cf06f7aeb0bb5b1c", "bytes_per_launch": 2 * (270.866688e6 + 50.163968e6)},
+    "attn_fwd_kernel": {"source_sha": "a3cb2cda04f85fb5", "bytes_per_launch": 2 * (201.526272e6 + 49.973760e6)},
 }
 
 
