@@ -69,8 +69,12 @@ struct Cfg {
   static constexpr int K_BYTES = QCH * kChunk;
   static constexpr int V_BYTES = VCH * kChunk;
   static constexpr int SLOT = K_BYTES > V_BYTES ? K_BYTES : V_BYTES;
-  static constexpr int NSLOT = DQK <= 64 ? 8 : (DQK <= 128 ? 4 : 2);
-  static constexpr int BAR_OFF = QT * Q_BYTES + NSLOT * SLOT;
+  // d_qk = 192: K and V in rings of their own, two 48 KB K slots and one 32 KB V
+  // slot (barriers 0, 1 and 2), so that the next K is copied while the current
+  // S runs; otherwise one ring of NSLOT slots taking K and V in turn.
+  static constexpr bool SPLIT = DQK == 192;
+  static constexpr int NSLOT = SPLIT ? 3 : (DQK <= 64 ? 8 : 4);
+  static constexpr int BAR_OFF = QT * Q_BYTES + (SPLIT ? 2 * K_BYTES + V_BYTES : NSLOT * SLOT);
   static constexpr int SMEM = BAR_OFF + 256 + 1024;  // barriers + alignment slack
   static_assert(SMEM <= 232448, "shared memory budget");
   // Register split: warpgroup 0 (TMA, MMA, two idle warps) gives registers to
@@ -203,6 +207,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   const int nkv_max = max(nkv[0], nkv[1]);
+  // Ring position of copy u (K of step u / 2 when u is even, V when odd): its
+  // barrier pair, the how-manieth copy into that slot it is, and its address.
+  auto ring_slot = [](int u) -> int {
+    if constexpr (C::SPLIT) return (u & 1) ? 2 : (u >> 1) & 1;
+    else return u % C::NSLOT;
+  };
+  auto ring_use = [](int u) -> uint32_t {
+    if constexpr (C::SPLIT) return static_cast<uint32_t>((u & 1) ? (u >> 1) : (u >> 2));
+    else return static_cast<uint32_t>(u / C::NSLOT);
+  };
+  auto ring_addr = [&](int u) -> uint8_t* {
+    if constexpr (C::SPLIT) return sKV + ((u & 1) ? 2 * C::K_BYTES : ((u >> 1) & 1) * C::K_BYTES);
+    else return sKV + (u % C::NSLOT) * C::SLOT;
+  };
   const PollLimit poll_lim = DIAG ? PollLimit{a.spin_limit} : kNoPollLimit;  // of the waits below
 
   // Early copies by thread 0 for dense d_qk <= 128 without a score
@@ -267,18 +285,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // read while the Q copies fly: V from the fp16 copy, or the bf16 original
       const CUtensorMap* tmvv = v_is_f16(a) ? &tmv16 : &tmv;
       tma_prefetch_desc(tmvv);
-      int issued = (kEarlyK && nkv_max > 0) ? 1 : 0;
-      bool ok = true;
-      for (int j = 0; j < nkv_max && ok; ++j) {
-        const int kb = key_block(j);
-        for (int which = (kEarlyK && j == 0) ? 1 : 0; which < 2 && ok; ++which) {  // K0 may be copied already
-          const int u = 2 * j + which;
-          const int slot = u % C::NSLOT;
-          const uint32_t use = static_cast<uint32_t>(u / C::NSLOT);
+      if constexpr (C::SPLIT) {
+        // Split rings: K0, then K(j+1) before V(j), since a K slot frees a step
+        // before the V slot does.
+        int last_use[C::NSLOT];  // per slot, the latest copy issued into it (for the drain)
+#pragma unroll
+        for (int s2 = 0; s2 < C::NSLOT; ++s2) last_use[s2] = -1;
+        const int n_copies = 2 * nkv_max;
+        bool ok = true;
+        for (int n = 0; n < n_copies + 1 && ok; ++n) {
+          const int u = n == 0 ? 0 : ((n & 1) ? n + 1 : n - 1);
+          if (u >= n_copies) continue;  // K of the step past the last
+          const int slot = ring_slot(u);
+          const uint32_t use = ring_use(u);
           ok = mbar_wait(&bar->kv_empty[slot], (use & 1u) ^ 1u, a.status, 0x100 + slot);
           if (!ok) break;
-          uint8_t* dst = sKV + slot * C::SLOT;
-          if (which == 0) {
+          const int kb = key_block(u >> 1);
+          uint8_t* dst = ring_addr(u);
+          if ((u & 1) == 0) {
             mbar_arrive_expect_tx(&bar->kv_full[slot], C::K_BYTES);
             for (int c = 0; c < C::QCH; ++c)
               tma_load_4d(dst + c * kChunk, &tmk, &bar->kv_full[slot], c * C::QX, h, k_start + kb * BN, b);
@@ -287,13 +311,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < C::VCH; ++c)
               tma_load_4d(dst + c * kChunk, tmvv, &bar->kv_full[slot], c * 64, h, k_start + kb * BN, b);
           }
-          ++issued;
+          last_use[slot] = static_cast<int>(use);
         }
-      }
-      if (!ok) {
-        // Drain: wait (bounded) for the copies still in flight into this CTA's shared memory.
-        for (int u = issued - 1; u >= 0 && u >= issued - C::NSLOT; --u)
-          mbar_wait(&bar->kv_full[u % C::NSLOT], static_cast<uint32_t>(u / C::NSLOT) & 1u, nullptr, 0);
+        if (!ok) {
+          // Drain: wait (bounded) for the copies still in flight into this CTA's shared memory.
+#pragma unroll
+          for (int s2 = 0; s2 < C::NSLOT; ++s2)
+            if (last_use[s2] >= 0) mbar_wait(&bar->kv_full[s2], static_cast<uint32_t>(last_use[s2]) & 1u, nullptr, 0);
+        }
+      } else {  // one ring: K0, V0, K1, V1, ...
+        int issued = (kEarlyK && nkv_max > 0) ? 1 : 0;
+        bool ok = true;
+        for (int j = 0; j < nkv_max && ok; ++j) {
+          const int kb = key_block(j);
+          for (int which = (kEarlyK && j == 0) ? 1 : 0; which < 2 && ok; ++which) {  // K0 may be copied already
+            const int u = 2 * j + which;
+            const int slot = u % C::NSLOT;
+            const uint32_t use = static_cast<uint32_t>(u / C::NSLOT);
+            ok = mbar_wait(&bar->kv_empty[slot], (use & 1u) ^ 1u, a.status, 0x100 + slot);
+            if (!ok) break;
+            uint8_t* dst = sKV + slot * C::SLOT;
+            if (which == 0) {
+              mbar_arrive_expect_tx(&bar->kv_full[slot], C::K_BYTES);
+              for (int c = 0; c < C::QCH; ++c)
+                tma_load_4d(dst + c * kChunk, &tmk, &bar->kv_full[slot], c * C::QX, h, k_start + kb * BN, b);
+            } else {
+              mbar_arrive_expect_tx(&bar->kv_full[slot], C::V_BYTES);
+              for (int c = 0; c < C::VCH; ++c)
+                tma_load_4d(dst + c * kChunk, tmvv, &bar->kv_full[slot], c * 64, h, k_start + kb * BN, b);
+            }
+            ++issued;
+          }
+        }
+        if (!ok) {
+          // Drain: wait (bounded) for the copies still in flight into this CTA's shared memory.
+          for (int u = issued - 1; u >= 0 && u >= issued - C::NSLOT; --u)
+            mbar_wait(&bar->kv_full[u % C::NSLOT], static_cast<uint32_t>(u / C::NSLOT) & 1u, nullptr, 0);
+        }
       }
       mbar_wait(&bar->q_full[0], 0, nullptr, 0);
       mbar_wait(&bar->q_full[1], 0, nullptr, 0);
@@ -309,16 +363,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool haveK = j < nkv_max;
         const bool haveV = j > 0;
         const int uK = 2 * j, uV = 2 * (j - 1) + 1;
-        const int sK = uK % C::NSLOT, sV = (uV + C::NSLOT) % C::NSLOT;
+        const int sK = ring_slot(uK), sV = ring_slot(haveV ? uV : 1);
         const uint32_t js = (static_cast<uint32_t>(j) & 0xFFFu) << 12;  // the step, in the site's bits 12..23
-        if (haveK) ok = mbar_wait(&bar->kv_full[sK], static_cast<uint32_t>(uK / C::NSLOT) & 1u, a.status, 0x210 | js, poll_lim);
+        if (haveK) ok = mbar_wait(&bar->kv_full[sK], ring_use(uK) & 1u, a.status, 0x210 | js, poll_lim);
         if (ok && haveV)
-          ok = mbar_wait(&bar->kv_full[sV], static_cast<uint32_t>(uV / C::NSLOT) & 1u, a.status, 0x211 | js, poll_lim);
+          ok = mbar_wait(&bar->kv_full[sV], ring_use(uV) & 1u, a.status, 0x211 | js, poll_lim);
         if (!ok) break;
         tc_fence_after();
         // descriptors built once per tile, advanced per k-step with one add
-        const uint64_t dk = smem_desc(smem_u32(sKV + sK * C::SLOT), 16, 1024, SWZ_128B);
-        const uint64_t dv = smem_desc(smem_u32(sKV + sV * C::SLOT), kChunk, 1024, SWZ_128B);
+        const uint64_t dk = smem_desc(smem_u32(ring_addr(uK)), 16, 1024, SWZ_128B);
+        const uint64_t dv = smem_desc(smem_u32(ring_addr(haveV ? uV : 1)), kChunk, 1024, SWZ_128B);
 #pragma unroll
         for (int i = 0; i < QT; ++i) {
           if (haveV && j - 1 < nkv[i]) {
