@@ -386,6 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_ts(tbase + tO(i), tbase + tS(i) + kk * 8, desc_add(dv, kk * 2048), idO, kk > 0 ? 1u : acc0);
             }
             if (j == nkv[i]) mma_commit(&bar->o_full[i]);
+            // split rings: the V slot is free once the step's last PV (tile 1's,
+            // or tile 0's when tile 1 has no such step) has completed
+            if (C::SPLIT && (i == QT - 1 || j - 1 >= nkv[QT - 1])) mma_commit(&bar->kv_empty[sV]);
           }
           if (j < nkv[i]) {
             if (j == 0 && i > 0) {
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        if (haveV) mma_commit(&bar->kv_empty[sV]);
+        if (!C::SPLIT && haveV) mma_commit(&bar->kv_empty[sV]);
         if (haveK) mma_commit(&bar->kv_empty[sK]);
       }
       // Commits complete in order: once this one lands, every earlier MMA and
