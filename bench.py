@@ -56,7 +56,7 @@ KERNEL_SOURCES = {
 KERNEL_TRAFFIC_NCU = {
     "dkdv_wide_kernel": {"source_sha": "cf06f7aeb0bb5b1c", "bytes_per_launch": 2 * (270.809344e6 + 107.681024e6)},
     "dq_kernel": {"source_sha": "cf06f7aeb0bb5b1c", "bytes_per_launch": 2 * (270.866688e6 + 50.163968e6)},
-    "attn_fwd_kernel": {"source_sha": "a3cb2cda04f85fb5", "bytes_per_launch": 2 * (201.526272e6 + 49.973760e6)},
+    "attn_fwd_kernel": {"source_sha": "edb29ca6fe51fc21", "bytes_per_launch": 2 * (201.509888e6 + 49.095936e6)},
 }
 
 
