@@ -1211,29 +1211,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       for (int t = 0; t < T && ok; ++t) {
-        if (t + 1 < T) {  // next S, dP as soon as the softmax warps hold this tile's
-          ok = mbar_wait(&bar->sp_free, static_cast<uint32_t>(t) & 1u, a.status, 0x2215) && wait_stage(t + 1);
-          if (!ok) break;
+        auto issue_next = [&]() {  // S, dP of tile t + 1 into the regions the softmax warps have read
           tc_fence_after();
           issue_s(t + 1);
           issue_dp(t + 1);
           mma_commit(&bar->s_full);
           mma_commit(&bar->v_empty[(t + 1) % C::VST]);
-        }
-        ok = mbar_wait(&bar->ds_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2220);
-        if (!ok) break;
-        tc_fence_after();
-        const uint64_t mk = smem_desc(stage_k(t), KB * 128, 1024, SWZ_128B);
-        const uint32_t acc0 = t > 0 ? 1u : 0u;
-        // dQ += dS K: A = dS from TMEM (warpgroup w's 64 keys in columns tdS + [32w, 32w+32)),
-        // B = K tile read as [d][kv], MN-major
+        };
+        auto issue_dq = [&]() {
+          tc_fence_after();
+          const uint64_t mk = smem_desc(stage_k(t), KB * 128, 1024, SWZ_128B);
+          const uint32_t acc0 = t > 0 ? 1u : 0u;
+          // dQ += dS K: A = dS from TMEM (warpgroup w's 64 keys in columns tdS + [32w, 32w+32)),
+          // B = K tile read as [d][kv], MN-major
 #pragma unroll
-        for (int kk = 0; kk < KB / 16; ++kk) {
-          const uint32_t da = tbase + C::tdS + 32 * (kk / 4) + (kk % 4) * 8;
-          mma_ts(tbase + C::tdQ, da, desc_add(mk, kk * 2048), idQ, kk > 0 ? 1u : acc0);
+          for (int kk = 0; kk < KB / 16; ++kk) {
+            const uint32_t da = tbase + C::tdS + 32 * (kk / 4) + (kk % 4) * 8;
+            mma_ts(tbase + C::tdQ, da, desc_add(mk, kk * 2048), idQ, kk > 0 ? 1u : acc0);
+          }
+          mma_commit(&bar->ds_free);
+          mma_commit(&bar->k_empty[t % C::KST]);  // K(t) read for the last time: K(t + KST) may load
+        };
+        if constexpr (C::KST < 3) {
+          // Two K slots (d_qk = 192): K(t + 2) is copied only once dQ(t) has read K(t), so
+          // dQ(t) must not wait behind tile t + 1's S and dP when K(t + 1) is late.
+          // dQ(t) and S, dP(t + 1) touch disjoint TMEM and either order is valid:
+          // issue each as soon as its inputs are ready (bounded like mbar_wait).
+          const uint32_t ph = static_cast<uint32_t>(t) & 1u;
+          bool next_todo = t + 1 < T, dq_todo = true;
+          const uint64_t t0 = globaltimer_ns();
+          for (uint32_t polls = 0; (next_todo || dq_todo) && ok; ++polls) {
+            bool progressed = false;
+            if (next_todo && mbar_test(&bar->sp_free, ph) &&
+                mbar_test(&bar->k_full[(t + 1) % C::KST], static_cast<uint32_t>((t + 1) / C::KST) & 1u) &&
+                mbar_test(&bar->v_full[(t + 1) % C::VST], static_cast<uint32_t>((t + 1) / C::VST) & 1u)) {
+              issue_next();
+              next_todo = false;
+              progressed = true;
+            }
+            if (dq_todo && mbar_test(&bar->ds_full, ph)) {
+              issue_dq();
+              dq_todo = false;
+              progressed = true;
+            }
+            if (!progressed && (polls & 0xFFFu) == 0xFFFu) {
+              if (polls > (1u << 16) && *reinterpret_cast<volatile uint32_t*>(a.status) != 0) ok = false;
+              if (polls > kMinPolls && globaltimer_ns() - t0 > kWaitNs) {
+                record_error(a.status, DEV_TIMEOUT_MBAR, next_todo ? 0x2215 : 0x2220);
+                ok = false;
+              }
+            }
+          }
+          if (!ok) break;
+        } else {
+          if (t + 1 < T) {  // next S, dP as soon as the softmax warps hold this tile's
+            ok = mbar_wait(&bar->sp_free, static_cast<uint32_t>(t) & 1u, a.status, 0x2215) && wait_stage(t + 1);
+            if (!ok) break;
+            issue_next();
+          }
+          ok = mbar_wait(&bar->ds_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2220);
+          if (!ok) break;
+          issue_dq();
         }
-        mma_commit(&bar->ds_free);
-        mma_commit(&bar->k_empty[t % C::KST]);
       }
       mma_commit(&bar->acc_full);
       mma_commit(&bar->mma_done);
