@@ -54,9 +54,9 @@ KERNEL_SOURCES = {
                         "kernels.h"),
 }
 KERNEL_TRAFFIC_NCU = {
-    "dkdv_wide_kernel": {"source_sha": "cf06f7aeb0bb5b1c", "bytes_per_launch": 2 * (270.809344e6 + 107.681024e6)},
-    "dq_kernel": {"source_sha": "cf06f7aeb0bb5b1c", "bytes_per_launch": 2 * (270.866688e6 + 50.163968e6)},
-    "attn_fwd_kernel": {"source_sha": "edb29ca6fe51fc21", "bytes_per_launch": 2 * (201.509888e6 + 49.095936e6)},
+    "dkdv_wide_kernel": {"source_sha": "b5253d74be4dd0ba", "bytes_per_launch": 2 * (271.328000e6 + 107.745024e6)},
+    "dq_kernel": {"source_sha": "b5253d74be4dd0ba", "bytes_per_launch": 2 * (270.585344e6 + 50.070272e6)},
+    "attn_fwd_kernel": {"source_sha": "c32f05514f97420e", "bytes_per_launch": 2 * (201.786368e6 + 48.820480e6)},
 }
 
 
