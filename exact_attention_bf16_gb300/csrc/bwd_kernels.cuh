@@ -1022,6 +1022,11 @@ struct DqCfg {
   // ahead (one K/V pair per step is more than an SM fetches in one step's time).
   static constexpr int KST = DQK == 64 ? 4 : DQK == 128 ? 3 : 2;
   static constexpr int VST = DQK == 64 ? 3 : DQK == 128 ? 2 : 1;
+  // d_qk = 192: S and dP hand off through barriers of their own (s_full, s_free;
+  // dp_full, dp_free), so the softmax warps start on S(t) while dP(t) runs and
+  // S(t+1) is issued once they hold S(t). At d_qk <= 128 both go together
+  // (s_full, sp_free), measured faster there.
+  static constexpr bool SPLIT_SDP = KST < 3;
   static constexpr int OFF_DO = Q_BYTES;
   static constexpr int OFF_K = OFF_DO + DO_BYTES;
   static constexpr int OFF_V = OFF_K + KST * K_BYTES;
@@ -1040,8 +1045,11 @@ struct DqBars {
   uint64_t k_empty[4];
   uint64_t v_full[3];
   uint64_t v_empty[3];
-  uint64_t s_full;
+  uint64_t s_full;    // S(t) (and, unless SPLIT_SDP, dP(t)) has landed
   uint64_t sp_free;   // softmax warps hold S(t), dP(t) in registers
+  uint64_t dp_full;   // SPLIT_SDP: dP(t) has landed
+  uint64_t s_free;    // SPLIT_SDP: softmax warps hold S(t) in registers
+  uint64_t dp_free;   // SPLIT_SDP: softmax warps hold dP(t) in registers
   uint64_t ds_free;   // dQ(t) has read dS(t)
   uint64_t ds_full;
   uint64_t acc_full;
@@ -1115,6 +1123,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bar->s_full, 1);
     mbar_init(&bar->sp_free, kSoftThreads / 32);
+    mbar_init(&bar->dp_full, 1);
+    mbar_init(&bar->s_free, kSoftThreads / 32);
+    mbar_init(&bar->dp_free, kSoftThreads / 32);
     mbar_init(&bar->ds_free, 1);
     mbar_init(&bar->ds_full, kSoftThreads / 32);  // one arrival per softmax warp
     mbar_init(&bar->acc_full, 1);
@@ -1199,15 +1210,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
+      auto commit_s = [&](int t) {  // SPLIT_SDP
+        tc_fence_after();
+        issue_s(t);
+        mma_commit(&bar->s_full);
+      };
+      auto commit_dp = [&](int t) {  // SPLIT_SDP
+        tc_fence_after();
+        issue_dp(t);
+        mma_commit(&bar->dp_full);
+        mma_commit(&bar->v_empty[t % C::VST]);  // V(t) has no other reader
+      };
       if (ok) ok = mbar_wait(&bar->q_full, 0, a.status, 0x2201);
       if (ok && T > 0) {
         ok = wait_stage(0);
         if (ok) {
-          tc_fence_after();
-          issue_s(0);
-          issue_dp(0);
-          mma_commit(&bar->s_full);
-          mma_commit(&bar->v_empty[0]);
+          if constexpr (C::SPLIT_SDP) {
+            commit_s(0);
+            commit_dp(0);
+          } else {
+            tc_fence_after();
+            issue_s(0);
+            issue_dp(0);
+            mma_commit(&bar->s_full);
+            mma_commit(&bar->v_empty[0]);
+          }
         }
       }
       for (int t = 0; t < T && ok; ++t) {
@@ -1232,21 +1259,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(&bar->ds_free);
           mma_commit(&bar->k_empty[t % C::KST]);  // K(t) read for the last time: K(t + KST) may load
         };
-        if constexpr (C::KST < 3) {
+        if constexpr (C::SPLIT_SDP) {
           // Two K slots (d_qk = 192): K(t + 2) is copied only once dQ(t) has read K(t), so
           // dQ(t) must not wait behind tile t + 1's S and dP when K(t + 1) is late.
-          // dQ(t) and S, dP(t + 1) touch disjoint TMEM and either order is valid:
+          // dQ(t), S(t + 1) and dP(t + 1) touch disjoint TMEM and any order is valid:
           // issue each as soon as its inputs are ready (bounded like mbar_wait).
           const uint32_t ph = static_cast<uint32_t>(t) & 1u;
-          bool next_todo = t + 1 < T, dq_todo = true;
+          bool s_todo = t + 1 < T, dp_todo = t + 1 < T, dq_todo = true;
           const uint64_t t0 = globaltimer_ns();
-          for (uint32_t polls = 0; (next_todo || dq_todo) && ok; ++polls) {
+          for (uint32_t polls = 0; (s_todo || dp_todo || dq_todo) && ok; ++polls) {
             bool progressed = false;
-            if (next_todo && mbar_test(&bar->sp_free, ph) &&
-                mbar_test(&bar->k_full[(t + 1) % C::KST], static_cast<uint32_t>((t + 1) / C::KST) & 1u) &&
+            if (s_todo && mbar_test(&bar->s_free, ph) &&
+                mbar_test(&bar->k_full[(t + 1) % C::KST], static_cast<uint32_t>((t + 1) / C::KST) & 1u)) {
+              commit_s(t + 1);
+              s_todo = false;
+              progressed = true;
+            }
+            if (dp_todo && mbar_test(&bar->dp_free, ph) &&
                 mbar_test(&bar->v_full[(t + 1) % C::VST], static_cast<uint32_t>((t + 1) / C::VST) & 1u)) {
-              issue_next();
-              next_todo = false;
+              commit_dp(t + 1);
+              dp_todo = false;
               progressed = true;
             }
             if (dq_todo && mbar_test(&bar->ds_full, ph)) {
@@ -1257,7 +1289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!progressed && (polls & 0xFFFu) == 0xFFFu) {
               if (polls > (1u << 16) && *reinterpret_cast<volatile uint32_t*>(a.status) != 0) ok = false;
               if (polls > kMinPolls && globaltimer_ns() - t0 > kWaitNs) {
-                record_error(a.status, DEV_TIMEOUT_MBAR, next_todo ? 0x2215 : 0x2220);
+                record_error(a.status, DEV_TIMEOUT_MBAR, s_todo ? 0x2215 : (dp_todo ? 0x2216 : 0x2220));
                 ok = false;
               }
             }
@@ -1309,47 +1341,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int cnt = lim - key_block(t) * KB;  // visible keys of this row in tile t
-      // copy this warpgroup's 64 columns of S and dP out of TMEM, then release dP
-      uint32_t s[64], dp[64];
-      tmem_ld32(lane_base + C::tS + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      tmem_ld32(lane_base + C::tS + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-      tmem_ld32(lane_base + C::tdP + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
-      tmem_ld32(lane_base + C::tdP + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar->sp_free);
-      uint32_t dw[32];
+      uint32_t s[64], dp[64], dw[32];
       // ALiBi: slope * (key - qpos) of this warpgroup's first key column
       const float abase = alibi_slope * static_cast<float>(key_block(t) * KB + wg * 64 - i - (U.nk - U.nq));
-      auto row = [&](bool mask) {
+      // P of columns e, e + 1 (zero where masked) and the score modification's derivative f there
+      auto prob2 = [&](int e, bool mask, float2& f) -> float2 {
+        const int col = wg * 64 + e;
+        float s0 = __uint_as_float(s[e]), s1 = __uint_as_float(s[e + 1]);
+        f = make_float2(1.f, 1.f);
+        if constexpr (MOD == kModSoftcap) {
+          const float t0 = tanh_scaled(s0, a.mod_k2), t1 = tanh_scaled(s1, a.mod_k2);
+          s0 = a.mod_b * t0;
+          s1 = a.mod_b * t1;
+          f = make_float2(fmaf(-t0, t0, 1.f), fmaf(-t1, t1, 1.f));
+        } else if constexpr (MOD == kModAlibi) {
+          s0 -= fabsf(fmaf(alibi_slope, static_cast<float>(e), abase));
+          s1 -= fabsf(fmaf(alibi_slope, static_cast<float>(e + 1), abase));
+        }
+        const float2 x = ffma2(make_float2(s0, s1), sl2v, nl);
+        float2 p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
+        if (mask) {
+          if (col >= cnt) p.x = 0.f;
+          if (col + 1 >= cnt) p.y = 0.f;
+        }
+        return p;
+      };
+      const bool full = cnt >= wg * 64 + 64;  // every key of this warpgroup's half is visible
+      if constexpr (C::SPLIT_SDP) {
+        // this warpgroup's 64 columns of S out of TMEM, then S released
+        tmem_ld32(lane_base + C::tS + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tmem_ld32(lane_base + C::tS + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar->s_free);
+        // P times f, in place of S, while dP(t) runs
+        auto prob = [&](bool mask) {
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          const int col = wg * 64 + e;
-          float s0 = __uint_as_float(s[e]), s1 = __uint_as_float(s[e + 1]);
-          float2 f = make_float2(1.f, 1.f);  // derivative of the score modification
-          if constexpr (MOD == kModSoftcap) {
-            const float t0 = tanh_scaled(s0, a.mod_k2), t1 = tanh_scaled(s1, a.mod_k2);
-            s0 = a.mod_b * t0;
-            s1 = a.mod_b * t1;
-            f = make_float2(fmaf(-t0, t0, 1.f), fmaf(-t1, t1, 1.f));
-          } else if constexpr (MOD == kModAlibi) {
-            s0 -= fabsf(fmaf(alibi_slope, static_cast<float>(e), abase));
-            s1 -= fabsf(fmaf(alibi_slope, static_cast<float>(e + 1), abase));
+          for (int e = 0; e < 64; e += 2) {
+            float2 f;
+            float2 p = prob2(e, mask, f);
+            if constexpr (MOD == kModSoftcap) p = fmul2(p, f);
+            s[e] = __float_as_uint(p.x);
+            s[e + 1] = __float_as_uint(p.y);
           }
-          const float2 x = ffma2(make_float2(s0, s1), sl2v, nl);
-          float2 p = make_float2(ex2_mufu(x.x), ex2_mufu(x.y));
-          if (mask) {
-            if (col >= cnt) p.x = 0.f;
-            if (col + 1 >= cnt) p.y = 0.f;
-          }
-          float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
-          if constexpr (MOD == kModSoftcap) ds = fmul2(ds, f);
+        };
+        if (full) prob(false);
+        else prob(true);
+        ok = mbar_wait_warp(&bar->dp_full, static_cast<uint32_t>(t) & 1u, a.status, 0x2302);
+        if (!ok) break;
+        tc_fence_after();
+        tmem_ld32(lane_base + C::tdP + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+        tmem_ld32(lane_base + C::tdP + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar->dp_free);
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {  // dS = P f (dP - D)
+          const float2 ds = fmul2(make_float2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
+                                  fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
           dw[e / 2] = pack_bf16x2(ds.x, ds.y);
         }
-      };
-      if (cnt >= wg * 64 + 64) row(false);  // every key of this warpgroup's half is visible
-      else row(true);
+      } else {
+        // this warpgroup's 64 columns of S and dP out of TMEM, then both released
+        tmem_ld32(lane_base + C::tS + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tmem_ld32(lane_base + C::tS + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        tmem_ld32(lane_base + C::tdP + wg * 64, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+        tmem_ld32(lane_base + C::tdP + wg * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar->sp_free);
+        auto row = [&](bool mask) {  // dS = P (dP - D) f
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            float2 f;
+            const float2 p = prob2(e, mask, f);
+            float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd));
+            if constexpr (MOD == kModSoftcap) ds = fmul2(ds, f);
+            dw[e / 2] = pack_bf16x2(ds.x, ds.y);
+          }
+        };
+        if (full) row(false);
+        else row(true);
+      }
       if (t > 0) {  // dQ(t-1) must have read the previous dS
         ok = mbar_wait_warp(&bar->ds_free, static_cast<uint32_t>(t - 1) & 1u, a.status, 0x2305);
         if (!ok) break;
