@@ -5,7 +5,8 @@ give exactly the gradients of attn_bwd with a caller-provided workspace (the
 same kernels run, and both are bitwise reproducible), on two calls in a row
 (the second reuses the library's fixed scratch array left over from the
 first), dense and packed variable-length, in both modes, and must refuse
-problems larger than that array.
+problems larger than that array. The dense gradients are also compared with
+the fp64 oracle on one (batch, head) pair.
 
 This file is named so that pytest collects it last."""
 import ctypes
@@ -14,6 +15,8 @@ import pytest
 import torch
 
 import workloads
+from oracle import attention_bwd
+from parity import check_grads
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +57,11 @@ def test_noalloc_matches_workspace_entry_point(dims, causal, deterministic):
     torch.cuda.synchronize()
     _two_calls(lib, abi, lambda dq, dk, dv: _params(ea, abi, t, w, o, lse, dq, dk, dv, deterministic),
                (t["q"], t["k"], t["v"]), ref, f"dense {dims} causal={causal} det={deterministic}")
+    b, h = 1, 2  # the no-allocation gradients equal ref bit for bit (above); ref against the oracle
+    q, k, v, do = (t[n][b, :, h].cpu() for n in ("q", "k", "v", "do"))
+    want = attention_bwd(q, k, v, do, w.scale, causal)
+    check_grads({"dq": ref[0][b, :, h], "dk": ref[1][b, :, h], "dv": ref[2][b, :, h]}, want,
+                f"no-allocation dense {dims} causal={causal} det={deterministic} b{b} h{h}")
 
 
 def test_noalloc_varlen_matches_workspace_entry_point():
