@@ -54,8 +54,8 @@ KERNEL_SOURCES = {
                         "kernels.h"),
 }
 KERNEL_TRAFFIC_NCU = {
-    "dkdv_wide_kernel": {"source_sha": "594d9820ac9a8733", "bytes_per_launch": 2 * (270.706944e6 + 107.655424e6)},
-    "dq_kernel": {"source_sha": "594d9820ac9a8733", "bytes_per_launch": 2 * (270.584832e6 + 50.217216e6)},
+    "dkdv_wide_kernel": {"source_sha": "ed9207d05a97ad13", "bytes_per_launch": 2 * (270.802176e6 + 107.651840e6)},
+    "dq_kernel": {"source_sha": "ed9207d05a97ad13", "bytes_per_launch": 2 * (270.653952e6 + 50.453248e6)},
     "attn_fwd_kernel": {"source_sha": "c32f05514f97420e", "bytes_per_launch": 2 * (201.786368e6 + 48.820480e6)},
 }
 

@@ -1286,6 +1286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               dq_todo = false;
               progressed = true;
             }
+            if (!progressed && polls > (1u << 20)) __nanosleep(256);  // as mbar_wait: back off only when stuck
             if (!progressed && (polls & 0xFFFu) == 0xFFFu) {
               if (polls > (1u << 16) && *reinterpret_cast<volatile uint32_t*>(a.status) != 0) ok = false;
               if (polls > kMinPolls && globaltimer_ns() - t0 > kWaitNs) {
