@@ -276,8 +276,8 @@ def measure_configs(ea, dev, stream) -> dict:
     d=128 sequence sweep (B*N = 32768, both masks), the outlier variant, the
     forward with part of exp2 on the FMA pipe, the two score modifications,
     the forward on FP8 E4M3 inputs, the d=64 backward in its two-kernel and
-    single-pass forms, the (192,128) shape, the N=16384 training shape in both backward modes
-    and the 32-sequence varlen batch. Inputs stay resident; each number is a
+    single-pass forms, the (192,128) shape, the N=16384 training shape in both backward modes,
+    512 queries against 32768 keys (the split-key forward) and the 32-sequence varlen batch. Inputs stay resident; each number is a
     median of 5 launches."""
     import torch
     import workloads
@@ -384,6 +384,11 @@ def measure_configs(ea, dev, stream) -> dict:
     r = dense(w, modes=(False, True))
     rec("bwd_d128_B2_H16_N16384_causal", w, r["fwd"], r[False])
     rec("bwd_d128_B2_H16_N16384_causal_deterministic", w, None, r[True], deterministic=True)
+    for causal in (False, True):  # short queries against long keys: the forward splits its keys across CTAs
+        w = workloads.Workload(f"short_q{'_causal' if causal else ''}", 1, 16, 512, 32768, 128, 128, causal, seed=0)
+        r = dense(w)
+        rec(f"dense_d128_B1_H16_Nq512_Nk32768_{'causal' if causal else 'noncausal'}", w, r["fwd"], r[False],
+            kv_split=True)
 
     w = workloads.varlen_32seq()
     t = workloads.make_varlen(w, device=dev)

@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -281,7 +282,8 @@ size_t seq_scratch_bytes(int num_seqs) { return round256(static_cast<int64_t>(nu
 
 // Forward workspace: a 256-byte block holding the range flag, then the fp16
 // copy of V ([rows, heads, d_v], contiguous) that the PV product reads, then
-// (packed variable length) the tile list and its scratch.
+// (packed variable length) the tile list and its scratch, or (split keys) the
+// ranges' fp32 O and LSE.
 size_t fwd_v16_bytes(const attn_fwd_params* p, bool varlen) {
   if (p->heads < 1 || p->d_v <= 0) return 0;
   const int64_t rows = varlen ? static_cast<int64_t>(p->total_k) : static_cast<int64_t>(p->batch) * p->seqlen_k;
@@ -291,11 +293,47 @@ size_t fwd_v16_bytes(const attn_fwd_params* p, bool varlen) {
 ListPlan fwd_list_plan(const attn_fwd_params* p, bool varlen) {  // the pair forward takes no list
   return varlen && !p->cta_pair ? list_plan(p->total_q, p->num_seqs, p->heads, p->max_seqlen_q, 256) : ListPlan{};
 }
+// Split keys (dense): when the (query block, head, batch) grid would leave most
+// SMs idle and the keys are long, each 256-row block's keys are cut into
+// `splits` ranges of `per` 128-key blocks (at least kSplitMinBlocks each), one
+// CTA per range, and a second kernel merges the ranges (split-KV). A function of
+// the parameters alone, so the workspace size and the call agree.
+constexpr int64_t kSplitTargetCtas = 148;  // at most one wave (148 SMs on B200, 152 on GB300)
+constexpr int kSplitMinBlocks = 8;
+constexpr int kSplitMax = 32;              // one merge lane per range
+struct SplitPlan {
+  int splits = 1, per = 0;
+};
+SplitPlan fwd_split_plan(const attn_fwd_params* p, bool varlen) {
+  SplitPlan sp;
+  if (varlen || p->cta_pair || p->input_dtype != ATTN_INPUT_BF16 || p->score_mod != ATTN_SCORE_NONE ||
+      p->exp2_emu_period != 0 || p->d_qk != p->d_v || (p->d_qk != 64 && p->d_qk != 128))
+    return sp;
+  if (p->batch < 1 || p->heads < 1 || p->seqlen_q < 1 || p->seqlen_k < 1) return sp;
+  const int64_t ctas = static_cast<int64_t>(p->batch) * p->heads * ((p->seqlen_q + 255) / 256);
+  const int nkb = (p->seqlen_k + 127) / 128;
+  if (ctas * 2 > kSplitTargetCtas || nkb < 2 * kSplitMinBlocks) return sp;
+  // at most kSplitTargetCtas CTAs: a range count that spills a few CTAs into a
+  // second wave costs as much as a whole extra wave
+  int64_t s = std::min<int64_t>(kSplitTargetCtas / ctas, nkb / kSplitMinBlocks);
+  s = std::min<int64_t>(s, kSplitMax);
+  if (s < 2) return sp;
+  sp.per = static_cast<int>((nkb + s - 1) / s);
+  sp.splits = (nkb + sp.per - 1) / sp.per;  // no empty range
+  if (sp.splits < 2) sp = SplitPlan{};
+  return sp;
+}
+size_t fwd_split_bytes(const attn_fwd_params* p, const SplitPlan& sp) {
+  if (sp.splits < 2) return 0;
+  const int64_t rows = static_cast<int64_t>(p->batch) * p->heads * p->seqlen_q;
+  return round256(sp.splits * rows * p->d_v * 4) + round256(sp.splits * rows * 4);
+}
 size_t fwd_workspace_bytes(const attn_fwd_params* p, bool varlen) {
   const size_t v16 = fwd_v16_bytes(p, varlen);
   if (!v16) return 0;
   const ListPlan lp = fwd_list_plan(p, varlen);
-  return 256 + v16 + (lp.use ? lp.list_bytes + seq_scratch_bytes(p->num_seqs) : 0);
+  return 256 + v16 + (lp.use ? lp.list_bytes + seq_scratch_bytes(p->num_seqs) : 0) +
+         fwd_split_bytes(p, fwd_split_plan(p, varlen));
 }
 
 // diag_limit != 0: the diagnostic launch of attn_diag_wait_timeout instead of the forward.
@@ -427,6 +465,15 @@ attn_status_t run_fwd(const attn_fwd_params* p, bool varlen, cudaStream_t stream
     if (e != cudaSuccess) return cuda_fail(e, "fwd tile list");
     a.tiles = list;
     a.n_tiles = lp.bound;
+  }
+  const SplitPlan spl = (sp.kv_count || p->cta_pair || f8) ? SplitPlan{} : fwd_split_plan(p, varlen);
+  if (spl.splits > 1) {  // fp32 O and LSE of every key range, after the fp16 copy of V
+    uint8_t* pbase = static_cast<uint8_t*>(ws) + 256 + fwd_v16_bytes(p, varlen);
+    a.kv_split = spl.splits;
+    a.kv_blocks_per_split = spl.per;
+    a.part_rows = static_cast<int64_t>(p->batch) * p->heads * p->seqlen_q;
+    a.o_part = reinterpret_cast<float*>(pbase);
+    a.lse_part = reinterpret_cast<float*>(pbase + round256(spl.splits * a.part_rows * p->d_v * 4));
   }
   if (p->cta_pair) {
     CUtensorMap tk_h;  // 64-key boxes: each CTA of a pair loads half of every K tile

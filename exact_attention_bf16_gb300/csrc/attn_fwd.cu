@@ -30,11 +30,79 @@ __global__ void exp2_eval_kernel(const float* x, float* yp, float* yh, int64_t n
   }
 }
 
+// Merges the key ranges of a split forward: per row, LSE = ln sum_r exp(LSE_r) and
+// O = sum_r exp(LSE_r - LSE) O_r (the standard merge of partial softmax results over
+// disjoint key sets), the ranges taken in order, so the result does not depend on
+// timing. One warp per (batch, head, row); lane l holds columns [DV/32 l, DV/32 (l+1)).
+template <int DV>
+__global__ void combine_kv_splits_kernel(FwdArgs a) {
+  constexpr int CPL = DV / 32;
+  const int lane = static_cast<int>(threadIdx.x & 31u);
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t row = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; row < a.part_rows;
+       row += nwarps) {
+    const float lr = lane < a.kv_split ? a.lse_part[lane * a.part_rows + row] : -INFINITY;
+    float m = lr;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float w = (lr == -INFINITY) ? 0.f : expf(lr - m);
+    float wsum = w;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    float acc[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+    for (int r = 0; r < a.kv_split; ++r) {
+      const float wr = __shfl_sync(0xffffffffu, w, r);
+      if (wr == 0.f) continue;  // warp-uniform: a range with no visible key
+      const float* src = a.o_part + (r * a.part_rows + row) * DV + lane * CPL;
+      if constexpr (CPL == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] = fmaf(wr, v.x, acc[0]);
+        acc[1] = fmaf(wr, v.y, acc[1]);
+        acc[2] = fmaf(wr, v.z, acc[2]);
+        acc[3] = fmaf(wr, v.w, acc[3]);
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] = fmaf(wr, v.x, acc[0]);
+        acc[1] = fmaf(wr, v.y, acc[1]);
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const int64_t q = row % a.seqlen_q, bh = row / a.seqlen_q;
+    const int64_t h = bh % a.heads, b = bh / a.heads;
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) + b * a.o_sb + q * a.o_sn + h * a.o_sh + lane * CPL;
+    if constexpr (CPL == 4) {
+      *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                   pack_bf16x2(acc[2] * inv, acc[3] * inv));
+    } else {
+      *reinterpret_cast<uint32_t*>(orow) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+    if (lane == 0) a.lse[b * a.lse_sb + h * a.lse_sh + q] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+  }
+}
+
+template <int DV>
+cudaError_t launch_combine(const FwdArgs& a, cudaStream_t stream) {
+  if (a.kv_split < 2 || a.kv_split > 32 || a.part_rows <= 0) return cudaErrorInvalidValue;
+  const int64_t blocks = (a.part_rows + 7) / 8;  // 8 warps (rows) per block of 256
+  combine_kv_splits_kernel<DV><<<static_cast<unsigned>(blocks < 4864 ? blocks : 4864), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
 // exp2 split: every EMU-th column of a row goes to the FMA-pipe polynomial
 // (0 = all on the hardware unit). Built for 0, 4 and 8.
 template <int DQK, int DV>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tv16,
                      const FwdArgs& a, cudaStream_t stream) {
+  if (a.kv_split > 1) {  // split keys: dense d = 64 or 128, no exp2 emulation
+    if constexpr (DQK <= 128 && DQK == DV) {
+      if (a.emu_period != 0 || a.tiles != nullptr) return cudaErrorInvalidValue;
+      cudaError_t e = launch_e<DQK, DV, 0, false, false, false, kModNone, false, true>(tq, tk, tv, tv16, a, stream);
+      return e == cudaSuccess ? launch_combine<DV>(a, stream) : e;
+    }
+    return cudaErrorInvalidValue;
+  }
   if (a.tiles != nullptr) {
     switch (a.emu_period) {
       case 0: return launch_e<DQK, DV, 0, false, false, true>(tq, tk, tv, tv16, a, stream);

@@ -130,8 +130,13 @@ __device__ __forceinline__ int key_limit(int row, int nq, int nk, int causal) {
 // columns per k-step, the same 32 bytes of each swizzled row as a bf16 k-step);
 // their descale factors are folded into a.scale_log2 by the host, V is the
 // exact fp16 copy and O is multiplied by a.v_descale in the epilogue.
+//
+// SPLITKV (dense): the key blocks are cut into a.kv_split ranges of
+// a.kv_blocks_per_split; CTA (x, y) takes range y of the block that x names and
+// writes its normalised fp32 O and its LSE over that range to a.o_part and
+// a.lse_part ([range][batch, head, row]); combine_kv_splits_kernel merges them.
 template <int DQK, int DV, int EMU_PERIOD, bool SPARSE = false, bool DIAG = false, bool LIST = false, int MOD = 0,
-          bool F8 = false>
+          bool F8 = false, bool SPLITKV = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmv16,
@@ -148,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // a few heads' K/V in L2 (all heads' K/V together exceed it); within a head
   // the heaviest (last, under the causal mask) 256-row blocks come first.
   int mblk, h, q_start = 0, k_start = 0, nq = a.seqlen_q, nk = a.seqlen_k, b;
+  int kv_part = 0;  // SPLITKV: this CTA's key range
   if constexpr (LIST) {
     // packed variable length: this CTA's entry of the tile list (longest sequences first)
     const int4* te = reinterpret_cast<const int4*>(a.tiles + blockIdx.x);
@@ -155,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (t1.z < 0) return;  // an empty entry past the real ones
     q_start = t0.x, nq = t0.y, k_start = t0.z, nk = t0.w, h = t1.x, mblk = t1.y, b = 0;
   } else {
+    if constexpr (SPLITKV) kv_part = static_cast<int>(blockIdx.y);
     const GridSlot g = grid_slot(static_cast<int>(blockIdx.x), a.num_units * a.heads, a.n_mblk, a.n_groups);
     const int bh = g.pair;
     mblk = a.n_mblk - 1 - g.rank;
@@ -193,6 +200,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  // SPLITKV: key blocks [kb_lo, kb_lo + a.kv_blocks_per_split) only
+  const int kb_lo = SPLITKV ? kv_part * a.kv_blocks_per_split : 0;
+  if constexpr (SPLITKV) {
+#pragma unroll
+    for (int i = 0; i < QT; ++i) nkv[i] = max(0, min(nkv[i], kb_lo + a.kv_blocks_per_split) - kb_lo);
+  }
   // Key block of step j: j itself, or the j-th listed block. A listed index
   // outside [0, ceil(nk / BN)) becomes ceil(nk / BN), a block past the last
   // key: its loads read zeros and every key in it is masked. (Addresses and
@@ -203,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kb = __ldg(a.kv_index + (list_row * a.max_kv + j));
       return (kb < 0 || kb >= n_kblk) ? n_kblk : kb;
     } else {
-      return j;
+      return j + kb_lo;
     }
   };
   const int nkv_max = max(nkv[0], nkv[1]);
@@ -424,7 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t quarter = warp & 3u;    // TMEM lane quarter this warp may access
     const int row_in_tile = static_cast<int>(quarter * 32 + lane);
     const int row = row0 + i * BM + row_in_tile;
-    const int klim = key_limit(row, nq, nk, a.causal);  // keys visible to this row
+    // keys visible to this row (SPLITKV: counted from the range's first key, so that
+    // step j is key block j of the range and kb_lo need not stay live in the loop)
+    const int klim = key_limit(row, nq, nk, a.causal) - (SPLITKV ? kb_lo * BN : 0);
     const float alibi_slope = MOD == kModAlibi ? __ldg(a.alibi_slopes + h) * a.inv_scale : 0.f;  // raw units
     const int qpos = row + (nk - nq);  // the row's position among the keys (bottom-right aligned)
     const uint32_t lane_base = tbase + ((quarter * 32u) << 16);
@@ -435,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n_rescale = 0, n_opp = 0;
     bool ok = true;
     for (int j = 0; j < nkv[i]; ++j) {
-      const int kb = key_block(j);  // read before the wait, off the critical path
+      const int kb = SPLITKV ? j : key_block(j);  // read before the wait, off the critical path
       // site: 0x300 + tile, the step in bits 12..23 (a timeout then says where it stopped)
       ok = mbar_wait_warp(&bar->s_full[i], static_cast<uint32_t>(j) & 1u, a.status,
                           0x300u + i + ((static_cast<uint32_t>(j) & 0xFFFu) << 12), poll_lim);
@@ -543,9 +558,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     float inv_l = (l > 0.f) ? 1.f / l : 0.f;
     if constexpr (F8) inv_l *= a.v_descale;
+    const bool store = row < nq;
+    if constexpr (SPLITKV) {
+      // this range's O (normalised over its keys, fp32) and LSE; -inf where it has no key
+      const int64_t prow = static_cast<int64_t>(blockIdx.y) * a.part_rows +
+                           (static_cast<int64_t>(b) * a.heads + h) * a.seqlen_q + q_start + row;
+      float4* op = reinterpret_cast<float4*>(a.o_part + prow * DV);
+#pragma unroll
+      for (int c = 0; c < DV / 32; ++c) {
+        uint32_t o[32];
+        if (nkv[i] > 0) {
+          tmem_ld32(lane_base + tO(i) + c * 32, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) o[t] = 0u;
+        }
+        if (store) {
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            op[c * 8 + t] = make_float4(__uint_as_float(o[4 * t]) * inv_l, __uint_as_float(o[4 * t + 1]) * inv_l,
+                                        __uint_as_float(o[4 * t + 2]) * inv_l, __uint_as_float(o[4 * t + 3]) * inv_l);
+        }
+      }
+      if (store) a.lse_part[prow] = (l > 0.f) ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    } else {
     __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) + static_cast<int64_t>(b) * a.o_sb +
                           static_cast<int64_t>(q_start + row) * a.o_sn + static_cast<int64_t>(h) * a.o_sh;
-    const bool store = row < nq;
 #pragma unroll
     for (int c = 0; c < DV / 32; ++c) {
       uint32_t o[32];
@@ -566,6 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lse = (l > 0.f) ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
       a.lse[static_cast<int64_t>(b) * a.lse_sb + static_cast<int64_t>(h) * a.lse_sh + q_start + row] = lse;
     }
+    }
   }
 
   // ---- teardown ------------------------------------------------------------
@@ -576,11 +616,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int DQK, int DV, int EMU, bool SPARSE = false, bool DIAG = false, bool LIST = false, int MOD = 0,
-          bool F8 = false>
+          bool F8 = false, bool SPLITKV = false>
 cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tv16,
                      const FwdArgs& a, cudaStream_t stream) {
   using C = Cfg<DQK, DV, F8>;
-  auto kern = attn_fwd_kernel<DQK, DV, EMU, SPARSE, DIAG, LIST, MOD, F8>;
+  auto kern = attn_fwd_kernel<DQK, DV, EMU, SPARSE, DIAG, LIST, MOD, F8, SPLITKV>;
   static PerDeviceOnce once;
   cudaError_t e = once.run([&]() -> cudaError_t {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -593,12 +633,15 @@ cudaError_t launch_e(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   });
   if (e != cudaSuccess) return e;
   if (LIST != (a.tiles != nullptr) || MOD != a.score_mod || SPARSE != (a.kv_count != nullptr) ||
-      F8 != (a.input_e4m3 != 0))
+      F8 != (a.input_e4m3 != 0) || SPLITKV != (a.kv_split > 1))
+    return cudaErrorInvalidValue;
+  if (SPLITKV && (a.o_part == nullptr || a.lse_part == nullptr || a.kv_blocks_per_split < 1 || LIST || SPARSE))
     return cudaErrorInvalidValue;
   const int64_t grid = LIST ? a.n_tiles : static_cast<int64_t>(a.n_mblk) * a.num_units * a.heads;
   if (grid <= 0) return cudaSuccess;
-  if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM, stream>>>(tq, tk, tv, tv16, a);
+  if (grid > 0x7fffffff || (SPLITKV && a.kv_split > 65535)) return cudaErrorInvalidConfiguration;
+  const dim3 g3(static_cast<unsigned>(grid), SPLITKV ? static_cast<unsigned>(a.kv_split) : 1u);
+  kern<<<g3, kThreads, C::SMEM, stream>>>(tq, tk, tv, tv16, a);
   return cudaGetLastError();
 }
 

@@ -153,6 +153,13 @@ struct FwdArgs {
   // Dense launches (no tile list): dispatch groups of grid_slot; heads * num_units
   // gives the (unit, head)-major order.
   int n_groups;
+  // Split keys (dense, kv_split > 1): kv_split ranges of kv_blocks_per_split key
+  // blocks; range r writes O over its keys (fp32, normalised) to o_part and its LSE
+  // to lse_part, row (b * heads + h) * seqlen_q + i of range r at r * part_rows + row.
+  int kv_split, kv_blocks_per_split;
+  float* o_part;
+  float* lse_part;
+  int64_t part_rows;
 };
 
 cudaError_t launch_fwd(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -249,6 +249,16 @@ typedef struct attn_bwd_params {
  * instead. A variable-length forward that builds its tile list adds, each
  * rounded up to 256, 32 x heads x (total_q / 256 + num_seqs) bytes for the
  * list and 8 x num_seqs bytes of scratch.
+ * A dense forward (bf16, d_qk = d_v = 64 or 128, exp2_emu_period 0, no score
+ * modification, cta_pair 0) whose batch x heads x ceil(seqlen_q / 256) query
+ * blocks number at most 74 and whose keys span at least 16 blocks of 128
+ * splits its keys (split-KV): s = min(148 / blocks, key blocks / 8, 32)
+ * ranges of ceil(key blocks / s) blocks (then as many ranges as that needs),
+ * one CTA each, each writing O and LSE over its range, merged by a second
+ * kernel in range order. Its workspace then adds s x batch x heads x seqlen_q
+ * x (4 x d_v + 4) bytes (the two parts each rounded up to 256). The result
+ * equals the unsplit one within rounding and is the same bits on every call
+ * with the same shapes. The block-sparse forward never splits.
  * The backward's workspace holds D = rowsum(dO * O): 4 x heads x query rows
  * bytes, rounded up to 256, 16-byte aligned; a variable-length backward adds
  * its tile lists, 32 x heads x (total_k / 128 + num_seqs) bytes for dK/dV
