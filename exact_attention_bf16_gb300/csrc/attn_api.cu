@@ -531,6 +531,35 @@ size_t bwd_sem_bytes(const attn_bwd_params* p, bool varlen) {
   if (units < 0 || bwd_n_qt64(p, varlen) < 0) return 0;
   return round256(units * f.heads * bwd_n_qt64(p, varlen) * 4);
 }
+// Split keys for the dQ kernel (dense two-kernel backward): when the dQ grid's
+// batch x heads x ceil(seqlen_q / 128) query tiles would leave most SMs idle and
+// the keys are long, each tile's key blocks are cut into ranges as the forward
+// does (fwd_split_plan), one CTA per range, each writing its fp32 dQ partial;
+// a merge kernel adds them in range order. A function of the parameters alone.
+SplitPlan bwd_dq_split_plan(const attn_bwd_params* p, bool varlen) {
+  SplitPlan sp;
+  const attn_fwd_params& f = p->fwd;
+  if (varlen || p->single_pass || f.input_dtype != ATTN_INPUT_BF16) return sp;
+  if (!((f.d_qk == 64 && f.d_v == 64) || (f.d_qk == 128 && f.d_v == 128) || (f.d_qk == 192 && f.d_v == 128)))
+    return sp;
+  if (f.batch < 1 || f.heads < 1 || f.seqlen_q < 1 || f.seqlen_k < 1) return sp;
+  const int64_t ctas = static_cast<int64_t>(f.batch) * f.heads * ((f.seqlen_q + 127) / 128);
+  const int nkb = (f.seqlen_k + 127) / 128;
+  if (ctas * 2 > kSplitTargetCtas || nkb < 2 * kSplitMinBlocks) return sp;
+  int64_t s = std::min<int64_t>(kSplitTargetCtas / ctas, nkb / kSplitMinBlocks);
+  s = std::min<int64_t>(s, kSplitMax);
+  if (s < 2) return sp;
+  sp.per = static_cast<int>((nkb + s - 1) / s);
+  sp.splits = (nkb + sp.per - 1) / sp.per;
+  if (sp.splits < 2) sp = SplitPlan{};
+  return sp;
+}
+size_t bwd_dq_split_bytes(const attn_bwd_params* p, const SplitPlan& sp) {
+  if (sp.splits < 2) return 0;
+  const attn_fwd_params& f = p->fwd;
+  return round256(static_cast<int64_t>(sp.splits) * f.batch * f.heads * f.seqlen_q * f.d_qk * 4);
+}
+// The workspace without the split-key dQ partials (the least a call accepts).
 size_t bwd_workspace_bytes(const attn_bwd_params* p, bool varlen) {
   const size_t d = bwd_d_bytes(p, varlen);
   const size_t fused = bwd_dq_acc_bytes(p, varlen) + bwd_sem_bytes(p, varlen);
@@ -579,6 +608,9 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
   }
   const size_t need_d = bwd_workspace_bytes(p, varlen);
   const size_t need = need_d + (sp.kv_count ? bwd_sparse_extra_bytes(f, sp.lists_per_head) : 0);
+  // split-key dQ (after the rest of the workspace) only when the caller's workspace holds its partials
+  SplitPlan dqs = (sp.kv_count || nq_rows == 0 || nk_rows == 0) ? SplitPlan{} : bwd_dq_split_plan(p, varlen);
+  if (dqs.splits > 1 && ws_bytes < need + bwd_dq_split_bytes(p, dqs)) dqs = SplitPlan{};
   if (nq_rows > 0 && nk_rows > 0 && f.score_mod == ATTN_SCORE_ALIBI) ATTN_TRY(check_lists_device(f.q, {f.alibi_slopes}));
   if (nq_rows > 0 && nk_rows > 0 && (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u)))
     return ATTN_ERR_WORKSPACE;
@@ -709,13 +741,24 @@ attn_status_t run_bwd(const attn_bwd_params* p, void* ws, size_t ws_bytes, bool 
   }
   if (e == cudaSuccess) e = mark(1);
   if (e != cudaSuccess) return cuda_fail(e, "bwd dkdv launch");
+  if (dqs.splits > 1) {
+    a.dq_split = dqs.splits;
+    a.dq_kb_per_split = dqs.per;
+    a.dq_part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + need);
+  }
   e = launch_bwd_dq(f.d_qk, f.d_v, tq, tk, tv, tdo, a, stream);
+  if (e == cudaSuccess && dqs.splits > 1) e = launch_bwd_dq_merge(a, f.d_qk, stream);
   if (e == cudaSuccess) e = mark(2);
   if (e != cudaSuccess) return cuda_fail(e, "bwd dq launch");
   return ATTN_OK;
 }
 
 }  // namespace
+
+size_t bwd_workspace_min_size(const attn_bwd_params* p) {
+  return bwd_workspace_bytes(p, p->fwd.cu_seqlens_q != nullptr);
+}
+
 }  // namespace gb300
 
 using namespace gb300;
@@ -787,7 +830,8 @@ attn_status_t attn_bwd_block_sparse(const attn_bwd_params* p, const int32_t* kv_
 
 size_t attn_bwd_workspace_size(const attn_bwd_params* p) {
   if (!p) return 0;
-  return bwd_workspace_bytes(p, p->fwd.cu_seqlens_q != nullptr);
+  const bool varlen = p->fwd.cu_seqlens_q != nullptr;
+  return bwd_workspace_bytes(p, varlen) + bwd_dq_split_bytes(p, bwd_dq_split_plan(p, varlen));
 }
 
 attn_status_t attn_bwd(const attn_bwd_params* p, void* workspace, size_t workspace_bytes, attn_stream_t stream) {

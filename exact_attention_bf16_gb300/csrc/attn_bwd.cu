@@ -152,6 +152,55 @@ cudaError_t launch_bwd_dq(int d_qk, int d_v, const CUtensorMap& tq, const CUtens
   return cudaErrorInvalidValue;
 }
 
+namespace bwd {
+
+// Split-key dQ: dQ (bf16, strided) = scale * sum_r dq_part[r], the ranges added
+// in ascending order (so every call gives the same bits); one thread per 8
+// elements of a (batch, head, row).
+template <int D>
+__global__ void dq_merge_kernel(const BwdArgs a) {
+  constexpr int UPR = D / 8;
+  const int64_t rows = static_cast<int64_t>(a.batch) * a.heads * a.seqlen_q;  // ((b * heads + h) * seqlen_q + row)
+  const int64_t units = rows * UPR;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < units;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % UPR);
+    const int64_t rh = i / UPR;
+    const int row = static_cast<int>(rh % a.seqlen_q);
+    const int64_t bh = rh / a.seqlen_q;
+    const int h = static_cast<int>(bh % a.heads), b = static_cast<int>(bh / a.heads);
+    const float* src = a.dq_part + rh * D + 8 * c;
+    float4 x = __ldg(reinterpret_cast<const float4*>(src)), y = __ldg(reinterpret_cast<const float4*>(src) + 1);
+    for (int r = 1; r < a.dq_split; ++r) {
+      const float4* pr = reinterpret_cast<const float4*>(src + r * rows * D);
+      const float4 u = __ldg(pr), w = __ldg(pr + 1);
+      x = make_float4(x.x + u.x, x.y + u.y, x.z + u.z, x.w + u.w);
+      y = make_float4(y.x + w.x, y.y + w.y, y.z + w.z, y.w + w.w);
+    }
+    const float sc = a.scale;
+    const uint4 o = make_uint4(pack_bf16x2(x.x * sc, x.y * sc), pack_bf16x2(x.z * sc, x.w * sc),
+                               pack_bf16x2(y.x * sc, y.y * sc), pack_bf16x2(y.z * sc, y.w * sc));
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + b * a.dq_sb + static_cast<int64_t>(row) * a.dq_sn +
+                         h * a.dq_sh + 8 * c;
+    *reinterpret_cast<uint4*>(dst) = o;
+  }
+}
+
+}  // namespace bwd
+
+cudaError_t launch_bwd_dq_merge(const BwdArgs& a, int d_qk, cudaStream_t stream) {
+  if (a.dq_split < 2 || a.dq_part == nullptr || a.cu_q != nullptr) return cudaErrorInvalidValue;
+  const int64_t units = static_cast<int64_t>(a.batch) * a.heads * a.seqlen_q * (d_qk / 8);
+  if (units == 0) return cudaSuccess;
+  const int64_t want = (units + 255) / 256;
+  const unsigned blocks = static_cast<unsigned>(want < 152 * 16 ? want : 152 * 16);
+  if (d_qk == 64) bwd::dq_merge_kernel<64><<<blocks, 256, 0, stream>>>(a);
+  else if (d_qk == 128) bwd::dq_merge_kernel<128><<<blocks, 256, 0, stream>>>(a);
+  else if (d_qk == 192) bwd::dq_merge_kernel<192><<<blocks, 256, 0, stream>>>(a);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_zero(const BwdArgs& a, int d_qk, int d_v, bool zero_dq, bool zero_dkdv, cudaStream_t stream) {
   auto go = [&](void* p, int64_t sb, int64_t sn, int64_t sh, int nrows, int d) -> cudaError_t {
     const int64_t total = static_cast<int64_t>(a.batch) * nrows * a.heads;

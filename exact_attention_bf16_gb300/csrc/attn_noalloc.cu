@@ -29,6 +29,11 @@
 #include "../../include/attn.h"
 #include "kernels.h"
 
+namespace gb300 {
+// The backward's workspace without the optional split-key dQ partials.
+size_t bwd_workspace_min_size(const attn_bwd_params* p);
+}  // namespace gb300
+
 namespace {
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[ATTN_BWD_NOALLOC_SCRATCH_BYTES];
@@ -58,10 +63,12 @@ extern "C" attn_status_t attn_bwd_noalloc(const attn_bwd_params* p, attn_stream_
   const attn_fwd_params& f = p->fwd;
   const bool varlen = f.cu_seqlens_q != nullptr;
   // Shapes first: a negative size is a bad argument, not a problem too large
-  // for the scratch (attn_bwd_workspace_size reports 0 for it).
+  // for the scratch (the workspace size is 0 for it).
   if (f.heads < 1 || (varlen ? (f.total_q < 0 || f.total_k < 0) : (f.batch < 1 || f.seqlen_q < 0 || f.seqlen_k < 0)))
     return ATTN_ERR_INVALID_ARG;
-  const size_t need = attn_bwd_workspace_size(p);
+  // the workspace without the optional split-key dQ partials, which the
+  // backward uses only when the scratch also holds them
+  const size_t need = gb300::bwd_workspace_min_size(p);
   if (need > ATTN_BWD_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;  // problem too large for the fixed scratch
   const int nq = varlen ? f.total_q : f.seqlen_q;
   const int nk = varlen ? f.total_k : f.seqlen_k;

@@ -41,10 +41,12 @@ __device__ __forceinline__ Unit unit_bounds(const BwdArgs& a, int unit) {
 // (unit, head), blocks in descending (dQ: the last query blocks are the
 // heaviest under the causal mask) or ascending (dK/dV: the first key blocks)
 // order. Returns false for an empty list entry (the CTA has no work).
+// slot: the work item (blockIdx.x unless the kernel launches several CTAs per item).
 __device__ __forceinline__ bool bwd_work(const BwdArgs& a, const TileEntry* tiles, int nblk, bool descending,
-                                         Unit& U, int& h, int& blk) {
+                                         Unit& U, int& h, int& blk, int slot = -1) {
+  if (slot < 0) slot = static_cast<int>(blockIdx.x);
   if (tiles != nullptr) {
-    const int4* te = reinterpret_cast<const int4*>(tiles + blockIdx.x);
+    const int4* te = reinterpret_cast<const int4*>(tiles + slot);
     const int4 t0 = __ldg(te), t1 = __ldg(te + 1);
     if (t1.z < 0) return false;
     U = Unit{0, t0.x, t0.z, t0.y, t0.w, t1.z};
@@ -52,7 +54,7 @@ __device__ __forceinline__ bool bwd_work(const BwdArgs& a, const TileEntry* tile
     blk = t1.y;
     return true;
   }
-  const GridSlot g = grid_slot(static_cast<int>(blockIdx.x), a.num_units * a.heads, nblk, a.n_groups);
+  const GridSlot g = grid_slot(slot, a.num_units * a.heads, nblk, a.n_groups);
   const int bh = g.pair;
   blk = descending ? nblk - 1 - g.rank : g.rank;
   h = bh % a.heads;

@@ -1085,11 +1085,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (unit, head) slow for L2 sharing of K/V; heaviest (last) query tiles first within a head
   Unit U;
   int h, m;
-  if (!bwd_work(a, a.tiles_q, a.n_qblk, true, U, h, m)) return;
+  // split keys (dense, no block lists): range `split` of this query tile's key blocks
+  const bool split = !SPARSE && a.dq_split > 1;
+  const int range = split ? static_cast<int>(blockIdx.x % static_cast<unsigned>(a.dq_split)) : 0;
+  if (!bwd_work(a, a.tiles_q, a.n_qblk, true, U, h, m,
+                split ? static_cast<int>(blockIdx.x / static_cast<unsigned>(a.dq_split)) : -1))
+    return;
   const int q0 = m * MB;
   if (q0 >= U.nq) return;
   const int last = min(q0 + MB - 1, U.nq - 1);
   int T = ceil_div(key_limit(last, U.nq, U.nk, a.causal), KB);
+  const int kb0 = split ? range * a.dq_kb_per_split : 0;  // first key block of the range
+  if (split) T = max(0, min(T, kb0 + a.dq_kb_per_split) - kb0);
   // block-sparse: this query block's list (per (batch, head) or shared)
   const int64_t q_list = SPARSE ? (a.lists_per_head ? (static_cast<int64_t>(U.b) * a.heads + h) * a.n_qb256 : 0) +
                                       (q0 >> 8)
@@ -1105,7 +1112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kb = __ldg(a.kv_index + (q_list * a.max_kv + t));
       return (kb < 0 || kb >= n_kb) ? n_kb : kb;
     } else {
-      return t;
+      return kb0 + t;
     }
   };
 
@@ -1445,6 +1452,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + U.b * a.dq_sb +
                          static_cast<int64_t>(U.q_start + i) * a.dq_sn + h * a.dq_sh;
     constexpr int CPW = DQK / 2;  // dQ columns per warpgroup (32, 64 or 96)
+    // split keys: this range's unscaled fp32 dQ row (zero when the range sees no key)
+    float* part = split ? a.dq_part + ((static_cast<int64_t>(range) * a.batch + U.b) * a.heads + h) *
+                                          static_cast<int64_t>(a.seqlen_q) * DQK +
+                              static_cast<int64_t>(i) * DQK
+                        : nullptr;
 #pragma unroll
     for (int c = 0; c < CPW / 32; ++c) {
       const int col0 = wg * CPW + c * 32;
@@ -1452,6 +1464,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (T > 0) {
         tmem_ld32(lane_base + C::tdQ + col0, v);
         tmem_wait_ld();
+      }
+      if (split) {
+        if (i < U.nq) {
+          float4* pv = reinterpret_cast<float4*>(part + col0);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            pv[e] = T > 0 ? make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                        __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        continue;
       }
 #pragma unroll
       for (int e = 0; e < 16; ++e)
@@ -1507,7 +1530,10 @@ cudaError_t launch_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   static PerDeviceOnce once;
   cudaError_t e = once.run([&] { return set_smem(kern, C::SMEM); });
   if (e != cudaSuccess) return e;
-  const int64_t grid = a.tiles_q ? a.n_tiles_q : static_cast<int64_t>(a.n_qblk) * a.num_units * a.heads;
+  const int split = (!SPARSE && a.dq_split > 1) ? a.dq_split : 1;
+  if (split > 1 && (a.tiles_q != nullptr || a.dq_part == nullptr || a.dq_kb_per_split < 1))
+    return cudaErrorInvalidValue;
+  const int64_t grid = (a.tiles_q ? a.n_tiles_q : static_cast<int64_t>(a.n_qblk) * a.num_units * a.heads) * split;
   if (grid <= 0) return cudaSuccess;
   if (grid > 0x7fffffff) return cudaErrorInvalidConfiguration;
   kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM, stream>>>(tq, tk, tv, tdo, a);

@@ -257,6 +257,15 @@ struct BwdArgs {
   // Dense launches (no tile list): dispatch groups of grid_slot, for the dK/dV
   // and the dQ kernels; heads * num_units gives the (unit, head)-major order.
   int n_groups;
+  // Split keys for the dQ kernel (dense, no block lists; dq_split <= 1 means
+  // none): each 128-query tile's key blocks are cut into dq_split ranges of
+  // dq_kb_per_split blocks, one CTA each (range fastest in the grid), which
+  // stores its unscaled fp32 dQ over that range to
+  // dq_part[(range * batch * heads + b * heads + h) * seqlen_q + row][d_qk];
+  // launch_bwd_dq_merge adds the ranges in order and writes dQ.
+  int dq_split;
+  int dq_kb_per_split;
+  float* dq_part;
 };
 
 // Single-pass backward (d_qk = d_v = 64): dK, dV and the fp32 dQ partials of
@@ -287,6 +296,8 @@ cudaError_t launch_bwd_dkdv_pair(const CUtensorMap& tq_r, const CUtensorMap& tq_
 cudaError_t launch_bwd_transpose_lists(const BwdArgs& a, int n_kb, cudaStream_t stream);
 cudaError_t launch_bwd_dq(int d_qk, int d_v, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+// dQ (bf16, strided) = scale * (sum over r < a.dq_split, in order, of a.dq_part's range r).
+cudaError_t launch_bwd_dq_merge(const BwdArgs& a, int d_qk, cudaStream_t stream);
 // Zero-fills dQ, dK, dV rows of a problem with no keys or no queries.
 cudaError_t launch_bwd_zero(const BwdArgs& a, int d_qk, int d_v, bool zero_dq, bool zero_dkdv, cudaStream_t stream);
 

@@ -263,7 +263,17 @@ typedef struct attn_bwd_params {
  * bytes, rounded up to 256, 16-byte aligned; a variable-length backward adds
  * its tile lists, 32 x heads x (total_k / 128 + num_seqs) bytes for dK/dV
  * (none with cta_pair) and 32 x heads x (total_q / 128 + num_seqs) for dQ, and
- * 8 x num_seqs bytes of scratch, each rounded up to 256. */
+ * 8 x num_seqs bytes of scratch, each rounded up to 256.
+ * A dense two-kernel backward (bf16, single_pass 0, any supported head size,
+ * with or without a score modification) whose batch x heads x
+ * ceil(seqlen_q / 128) query tiles number at most 74 and whose keys span at
+ * least 16 blocks of 128 splits the keys of its dQ kernel by the forward's
+ * rule over those tiles: s = min(148 / tiles, key blocks / 8, 32) ranges, one
+ * CTA each, each storing its fp32 dQ over its range, added in range order by a
+ * second kernel (the same bits on every call; dK and dV are unchanged). The
+ * size then adds s x batch x heads x seqlen_q x d_qk x 4 bytes, rounded up to
+ * 256. A call given at least the size without those bytes (but less than the
+ * full size) runs unsplit. The block-sparse backward never splits. */
 size_t attn_fwd_workspace_size(const attn_fwd_params* p);
 size_t attn_bwd_workspace_size(const attn_bwd_params* p);
 
@@ -322,8 +332,10 @@ attn_status_t attn_bwd_block_sparse(const attn_bwd_params* p, const int32_t* kv_
  * no workspace: the scratch lives in a fixed array inside the library of
  * ATTN_BWD_NOALLOC_SCRATCH_BYTES bytes per GPU that loads the library, held
  * until process exit. The attention method has no counterpart to this entry
- * point; it exists only for these callers. Limit: attn_bwd_workspace_size(p)
- * must not exceed ATTN_BWD_NOALLOC_SCRATCH_BYTES (4 bytes per batch x head x
+ * point; it exists only for these callers. Limit: the workspace that
+ * attn_bwd would need, without the split-key dQ partials (which it uses only
+ * when the array also holds them), must not exceed
+ * ATTN_BWD_NOALLOC_SCRATCH_BYTES (4 bytes per batch x head x
  * query row, so up to 2,097,152 such rows dense; variable length adds the
  * tile lists), else ATTN_ERR_WORKSPACE and
  * nothing is launched. The first call on each device resolves the array's
