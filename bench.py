@@ -54,9 +54,9 @@ KERNEL_SOURCES = {
                         "kernels.h"),
 }
 KERNEL_TRAFFIC_NCU = {
-    "dkdv_wide_kernel": {"source_sha": "ed9207d05a97ad13", "bytes_per_launch": 2 * (270.802176e6 + 107.651840e6)},
-    "dq_kernel": {"source_sha": "ed9207d05a97ad13", "bytes_per_launch": 2 * (270.653952e6 + 50.453248e6)},
-    "attn_fwd_kernel": {"source_sha": "c32f05514f97420e", "bytes_per_launch": 2 * (201.786368e6 + 48.820480e6)},
+    "dkdv_wide_kernel": {"source_sha": "6517ab8c11a089ab", "bytes_per_launch": 2 * (270.730752e6 + 107.614720e6)},
+    "dq_kernel": {"source_sha": "6517ab8c11a089ab", "bytes_per_launch": 2 * (270.588928e6 + 50.289152e6)},
+    "attn_fwd_kernel": {"source_sha": "3484d0e8f058a718", "bytes_per_launch": 2 * (201.458944e6 + 49.052160e6)},
 }
 
 
