@@ -614,6 +614,16 @@ struct DkdvWBars {
 };
 static_assert(sizeof(DkdvWBars) <= 256, "dK/dV barriers must fit their reserved bytes");
 
+// Slot of query q (0..127) in a (-LSE*log2e) or (-D) vector of the wide dK/dV
+// kernel's ring. Within each 64-query half, queries 8r + 2c + j and
+// 8(r + 4) + 2c + j (r < 4, c < 4, j < 2) share the 16 bytes at slot
+// 16r + 4c, so the thread with fragment column pair c reads its 16 queries'
+// values in four 16-byte loads, a warp's four addresses spanning 64 bytes.
+__device__ __forceinline__ int vec_slot(int q) {
+  const int r = (q >> 3) & 7, c = (q >> 1) & 3, j = q & 1;
+  return (q & 64) + ((r & 3) * 4 + c) * 4 + (r >> 2) * 2 + j;
+}
+
 template <bool SPARSE = false, int MOD = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_wide_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -741,8 +751,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* vec = sVec + vs * 2 * QB;
 #pragma unroll
       for (int u = 0; u < QB / 32; ++u) {
-        vec[lane + 32 * u] = nl[u];
-        vec[QB + lane + 32 * u] = nd[u];
+        const int p = vec_slot(static_cast<int>(lane) + 32 * u);
+        vec[p] = nl[u];
+        vec[QB + p] = nd[u];
       }
       mbar_arrive(&bar->v_full[vs]);
     }
@@ -871,12 +882,16 @@ __global__ void __launch_bounds__(kThreads, 1)
            mbar_wait_warp(&bar->v_full[t % C::NVEC], static_cast<uint32_t>(t / C::NVEC) & 1u, a.status, 0x1431);
       if (!ok) break;
       tc_fence_after();
-      const float* vL = sVec + (t % C::NVEC) * 2 * QB + 64 * wg + 2 * c;
-      const float* vD = vL + QB;
+      const float4* vL = reinterpret_cast<const float4*>(sVec + (t % C::NVEC) * 2 * QB + 64 * wg) + c;
+      const float4* vD = vL + QB / 4;
       const bool full = all_keys && q0 >= vis_max;  // every (key, query) cell of this thread is visible
       float2 nlv[8];  // -LSE*log2e of this thread's 16 queries (the same for both lane groups)
 #pragma unroll
-      for (int r = 0; r < 8; ++r) nlv[r] = *reinterpret_cast<const float2*>(vL + 8 * r);
+      for (int r = 0; r < 4; ++r) {  // queries 8r + 2c, +1 and 8(r + 4) + 2c, +1 in one 16-byte load
+        const float4 x = vL[4 * r];
+        nlv[r] = make_float2(x.x, x.y);
+        nlv[r + 4] = make_float2(x.z, x.w);
+      }
       float p[2][32];
 #pragma unroll
       for (int lg = 0; lg < 2; ++lg) {
@@ -943,7 +958,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bar->sp_free);
       float2 ndv[8];  // -D of the same 16 queries
 #pragma unroll
-      for (int r = 0; r < 8; ++r) ndv[r] = *reinterpret_cast<const float2*>(vD + 8 * r);
+      for (int r = 0; r < 4; ++r) {
+        const float4 x = vD[4 * r];
+        ndv[r] = make_float2(x.x, x.y);
+        ndv[r + 4] = make_float2(x.z, x.w);
+      }
 #pragma unroll
       for (int lg = 0; lg < 2; ++lg) {
         uint32_t dw[16];
