@@ -54,8 +54,8 @@ KERNEL_SOURCES = {
                         "kernels.h"),
 }
 KERNEL_TRAFFIC_NCU = {
-    "dkdv_wide_kernel": {"source_sha": "6517ab8c11a089ab", "bytes_per_launch": 2 * (270.730752e6 + 107.614720e6)},
-    "dq_kernel": {"source_sha": "6517ab8c11a089ab", "bytes_per_launch": 2 * (270.588928e6 + 50.289152e6)},
+    "dkdv_wide_kernel": {"source_sha": "0e5c13170f822e3d", "bytes_per_launch": 2 * (270.638848e6 + 107.483392e6)},
+    "dq_kernel": {"source_sha": "0e5c13170f822e3d", "bytes_per_launch": 2 * (270.719488e6 + 50.029568e6)},
     "attn_fwd_kernel": {"source_sha": "3484d0e8f058a718", "bytes_per_launch": 2 * (201.458944e6 + 49.052160e6)},
 }
 
